@@ -1,0 +1,219 @@
+/*
+ * oracle.c -- plain float64 CPU reference for the exact attention forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this code.  It shares nothing with
+ * the CUDA library (no headers, helpers, tables or constants).
+ *
+ * What it computes is the textbook definition that the FlashAttention pages
+ * say the fused kernels reproduce exactly ("FlashAttention -- one, two,
+ * three!", section "Standard Attention"; comrad404 review, "Коротко" and FAQ):
+ *
+ *   s_ij  = scale * sum_c q_ic k_jc          for keys j < N (causal: j <= i)
+ *   m_i   = max_j s_ij
+ *   l_i   = sum_j exp(s_ij - m_i)
+ *   o_ic  = sum_j exp(s_ij - m_i) v_jc / l_i
+ *   lse_i = m_i + ln l_i
+ *
+ * Each query row is independent, so rows are spread over POSIX threads; every
+ * row is computed whole (no blocking, no online softmax).
+ *
+ * FP8 helpers follow the OCP 8-bit floating point specification for E4M3
+ * (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits, subnormals,
+ * S.1111.111 is NaN, no infinities, largest finite 448), plus the two
+ * pre-processing steps named in "Incoherent Processing for FP8 Accuracy"
+ * (FlashAttention-3 podcast page) and "Метод", item 3 (comrad404 review):
+ * a random-sign Hadamard rotation of Q and K, and block quantisation.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#define ORACLE_API __attribute__((visibility("default")))
+
+/* ---------------------------------------------------------------- attention */
+
+typedef struct {
+    const double *q, *k, *v;
+    double *o, *lse;
+    int64_t BH, N, d, R;        /* R = number of rows computed per head */
+    const int64_t *rows;         /* NULL: rows 0..N-1 */
+    int causal;
+    double scale;
+    int tid, nthreads;
+    int status;
+} att_job;
+
+static void *att_worker(void *arg) {
+    att_job *J = (att_job *)arg;
+    double *w = (double *)malloc(sizeof(double) * (size_t)J->N);
+    if (!w) { J->status = 1; return NULL; }
+    const int64_t total = J->BH * J->R;
+    for (int64_t item = J->tid; item < total; item += J->nthreads) {
+        const int64_t bh = item / J->R, r = item % J->R;
+        const int64_t i = J->rows ? J->rows[r] : r;          /* query row index */
+        const double *qi = J->q + (bh * J->N + i) * J->d;
+        const double *kh = J->k + bh * J->N * J->d;
+        const double *vh = J->v + bh * J->N * J->d;
+        const int64_t nkeys = J->causal ? i + 1 : J->N;      /* keys 0..nkeys-1 */
+        double m = -INFINITY;
+        for (int64_t j = 0; j < nkeys; ++j) {
+            double dot = 0.0;
+            for (int64_t c = 0; c < J->d; ++c) dot += qi[c] * kh[j * J->d + c];
+            w[j] = J->scale * dot;
+            if (w[j] > m) m = w[j];
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < nkeys; ++j) {
+            w[j] = exp(w[j] - m);
+            l += w[j];
+        }
+        double *oi = J->o + (bh * J->R + r) * J->d;
+        for (int64_t c = 0; c < J->d; ++c) oi[c] = 0.0;
+        for (int64_t j = 0; j < nkeys; ++j)
+            for (int64_t c = 0; c < J->d; ++c) oi[c] += w[j] * vh[j * J->d + c];
+        for (int64_t c = 0; c < J->d; ++c) oi[c] /= l;
+        if (J->lse) J->lse[bh * J->R + r] = m + log(l);
+    }
+    free(w);
+    return NULL;
+}
+
+/* q, k, v: [BH, N, d] float64.  o: [BH, R, d], lse: [BH, R] (may be NULL),
+ * where R = nrows if rows != NULL (row indices in [0, N)), else N.
+ * nthreads <= 0 uses every online core.  Returns 0 on success; writes the
+ * number of threads used to *threads_used (may be NULL). */
+ORACLE_API int oracle_attention(const double *q, const double *k, const double *v,
+                                double *o, double *lse, int64_t BH, int64_t N, int64_t d,
+                                int causal, double scale, const int64_t *rows, int64_t nrows,
+                                int nthreads, int *threads_used) {
+    if (!q || !k || !v || !o || BH < 0 || N < 0 || d < 1) return 2;
+    const int64_t R = rows ? nrows : N;
+    for (int64_t r = 0; rows && r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= N) return 2;
+    if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+    if (nthreads < 1) nthreads = 1;
+    if (BH * R < nthreads) nthreads = (int)(BH * R > 0 ? BH * R : 1);
+    if (threads_used) *threads_used = nthreads;
+    att_job *jobs = (att_job *)calloc((size_t)nthreads, sizeof(att_job));
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !th) { free(jobs); free(th); return 1; }
+    for (int t = 0; t < nthreads; ++t) {
+        att_job J = {q, k, v, o, lse, BH, N, d, R, rows, causal, scale, t, nthreads, 0};
+        jobs[t] = J;
+    }
+    int st = 0;
+    for (int t = 1; t < nthreads; ++t)
+        if (pthread_create(&th[t], NULL, att_worker, &jobs[t]) != 0) { jobs[t].status = 1; th[t] = 0; }
+    att_worker(&jobs[0]);
+    for (int t = 1; t < nthreads; ++t)
+        if (th[t]) pthread_join(th[t], NULL);
+    for (int t = 0; t < nthreads; ++t) st |= jobs[t].status;
+    free(jobs);
+    free(th);
+    return st;
+}
+
+/* ------------------------------------------------------------ E4M3 codec */
+
+ORACLE_API double oracle_e4m3_decode1(uint8_t code) {
+    const int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double mag;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) mag = ldexp((double)m / 8.0, -6);          /* subnormal: 0.m * 2^-6 */
+    else mag = ldexp(1.0 + (double)m / 8.0, e - 7);        /* normal: 1.m * 2^(e-7) */
+    return sign ? -mag : mag;
+}
+
+/* Round to nearest, ties to even; finite values beyond 448 saturate to +-448;
+ * NaN maps to 0x7F. */
+ORACLE_API uint8_t oracle_e4m3_encode1(double x) {
+    if (isnan(x)) return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs(x);
+    if (a >= 448.0) return sign | 0x7E;
+    if (a < ldexp(1.0, -6)) {                 /* subnormal grid: multiples of 2^-9 */
+        double n = nearbyint(ldexp(a, 9));    /* ties to even (default FP mode) */
+        return sign | (uint8_t)n;             /* n == 8 is the smallest normal, code 0x08 */
+    }
+    int ex;
+    double fr = frexp(a, &ex);                /* a = fr * 2^ex, fr in [0.5, 1) */
+    int e = ex - 1;                           /* a = (2 fr) * 2^e, 2 fr in [1, 2) */
+    double mq = nearbyint((2.0 * fr - 1.0) * 8.0);
+    if (mq == 8.0) { mq = 0.0; e += 1; }
+    int biased = e + 7;
+    if (biased > 15 || (biased == 15 && mq == 7.0)) return sign | 0x7E;
+    return sign | (uint8_t)((biased << 3) | (int)mq);
+}
+
+ORACLE_API void oracle_e4m3_decode(const uint8_t *codes, double *out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_decode1(codes[i]);
+}
+
+ORACLE_API void oracle_e4m3_encode(const double *x, uint8_t *codes, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) codes[i] = oracle_e4m3_encode1(x[i]);
+}
+
+/* ------------------------------------------------------- Hadamard rotation */
+
+/* Sylvester Hadamard matrix entry: H[i][j] = (-1)^popcount(i & j). */
+ORACLE_API int oracle_hadamard_entry(int64_t i, int64_t j) {
+    return (__builtin_popcountll((unsigned long long)(i & j)) & 1) ? -1 : 1;
+}
+
+/* x: [BH, N, d] with d a power of two; signs: [H, d] (+-1), head h = bh % H.
+ * out_row = (x_row * sigma_h) . H_d / sqrt(d)   (a dense product, O(d^2)). */
+ORACLE_API int oracle_hadamard_rotate(const double *x, const int8_t *signs, double *out,
+                                      int64_t BH, int64_t H, int64_t N, int64_t d) {
+    if (d < 1 || (d & (d - 1)) || H < 1) return 2;
+    const double inv = 1.0 / sqrt((double)d);
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        const int8_t *sg = signs + (bh % H) * d;
+        for (int64_t n = 0; n < N; ++n) {
+            const double *xr = x + (bh * N + n) * d;
+            double *yr = out + (bh * N + n) * d;
+            for (int64_t j = 0; j < d; ++j) {
+                double acc = 0.0;
+                for (int64_t i = 0; i < d; ++i)
+                    acc += xr[i] * (double)sg[i] * (double)oracle_hadamard_entry(i, j);
+                yr[j] = acc * inv;
+            }
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------ block quantisation */
+
+/* x: [BH, N, d].  For every (bh, block of `block` rows) -- or for the whole
+ * tensor when per_tensor != 0 -- the scale is s = amax / 448 in float32 (1 when
+ * amax == 0) and each element is encoded as E4M3(x / s), the division and the
+ * rounding decision taken in float32.  scales: [BH, ceil(N / block)] float32,
+ * or a single float when per_tensor != 0. */
+ORACLE_API int oracle_block_quantize(const double *x, uint8_t *codes, float *scales,
+                                     int64_t BH, int64_t N, int64_t d, int64_t block,
+                                     int per_tensor) {
+    if (block < 1) return 2;
+    const int64_t nblk = per_tensor ? 1 : (N + block - 1) / block;
+    for (int64_t bh = 0; bh < (per_tensor ? 1 : BH); ++bh) {
+        for (int64_t b = 0; b < nblk; ++b) {
+            int64_t r0 = per_tensor ? 0 : bh * N + b * block;
+            int64_t r1 = per_tensor ? BH * N : bh * N + ((b + 1) * block < N ? (b + 1) * block : N);
+            float amax = 0.0f;
+            for (int64_t r = r0; r < r1; ++r)
+                for (int64_t c = 0; c < d; ++c) {
+                    float a = fabsf((float)x[r * d + c]);
+                    if (a > amax) amax = a;
+                }
+            float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+            if (per_tensor) scales[0] = s; else scales[bh * nblk + b] = s;
+            for (int64_t r = r0; r < r1; ++r)
+                for (int64_t c = 0; c < d; ++c)
+                    codes[r * d + c] = oracle_e4m3_encode1((double)((float)x[r * d + c] / s));
+        }
+    }
+    return 0;
+}

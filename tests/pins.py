@@ -1,0 +1,207 @@
+"""Checks that pin the float64 attention oracle to facts other than its own code.
+
+Every check takes ``attn(q, k, v, causal, scale, rows=None) -> (O, lse)`` on
+float64 [B, H, N, d] arrays, so the same checks run against the real oracle
+(tests/test_oracle_pins.py) and against deliberately broken copies of it
+(tests/test_oracle_mutants.py), which must each fail at least one check.
+
+Sources of truth (none of them is the oracle's formula retyped):
+
+* closed forms the definition reduces to: uniform softmax when every logit is
+  equal (Q = 0 or scale = 0), a single visible key in causal row 0, constant V;
+* invariants of softmax attention: weights are a probability vector (seen
+  through V = identity), joint permutation of keys and values, a per-row logit
+  shift, an orthogonal change of basis shared by Q and K;
+* a brute-force row-by-row evaluation in pure Python without max subtraction;
+* hand-worked examples stored in tests/golden/two_key_softmax.json.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _rand(shape, seed, scale=1.0):
+    return _rng(seed).standard_normal(shape) * scale
+
+
+def check_zero_query_is_mean(attn):
+    """Q = 0: every logit is 0, so O_i = mean of the visible V rows, lse_i = ln(#keys)."""
+    B, H, N, d = 2, 3, 37, 8
+    q = np.zeros((B, H, N, d))
+    k, v = _rand((B, H, N, d), 1), _rand((B, H, N, d), 2)
+    o, lse = attn(q, k, v, False, 0.7)
+    np.testing.assert_allclose(o, np.broadcast_to(v.mean(axis=2, keepdims=True), o.shape),
+                               rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, np.full((B, H, N), math.log(N)), rtol=0, atol=1e-12)
+    o, lse = attn(q, k, v, True, 0.7)
+    prefix = np.cumsum(v, axis=2) / np.arange(1, N + 1)[None, None, :, None]
+    np.testing.assert_allclose(o, prefix, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, np.broadcast_to(np.log(np.arange(1, N + 1)), lse.shape),
+                               rtol=0, atol=1e-12)
+
+
+def check_zero_scale_is_mean(attn):
+    """scale = 0 with arbitrary Q, K: the same uniform average."""
+    B, H, N, d = 1, 2, 19, 4
+    q, k, v = (_rand((B, H, N, d), s, 3.0) for s in (3, 4, 5))
+    o, lse = attn(q, k, v, False, 0.0)
+    np.testing.assert_allclose(o, np.broadcast_to(v.mean(axis=2, keepdims=True), o.shape),
+                               rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, math.log(N), rtol=0, atol=1e-12)
+
+
+def check_causal_row0(attn):
+    """Causal row 0 sees key 0 alone: O_0 = V_0 and lse_0 = its single logit."""
+    B, H, N, d = 2, 2, 33, 16
+    q, k, v = (_rand((B, H, N, d), s) for s in (6, 7, 8))
+    scale = 0.3
+    o, lse = attn(q, k, v, True, scale)
+    np.testing.assert_allclose(o[:, :, 0], v[:, :, 0], rtol=0, atol=1e-12)
+    single = scale * np.einsum("bhc,bhc->bh", q[:, :, 0], k[:, :, 0])
+    np.testing.assert_allclose(lse[:, :, 0], single, rtol=0, atol=1e-12)
+
+
+def check_constant_v(attn):
+    """V = c everywhere: every convex combination of V rows is c."""
+    B, H, N, d = 1, 2, 45, 8
+    q, k = _rand((B, H, N, d), 9, 2.0), _rand((B, H, N, d), 10, 2.0)
+    c = _rand((d,), 11)
+    v = np.broadcast_to(c, (B, H, N, d)).copy()
+    for causal in (False, True):
+        o, _ = attn(q, k, v, causal, 0.5)
+        np.testing.assert_allclose(o, np.broadcast_to(c, o.shape), rtol=0, atol=1e-12)
+
+
+def check_weights_are_probabilities(attn):
+    """V = identity (N = d) exposes the softmax weights as O: rows are probability
+    vectors, and under the causal mask the weights above the diagonal are 0."""
+    N = 24
+    q, k = _rand((1, 2, N, N), 12), _rand((1, 2, N, N), 13)
+    v = np.broadcast_to(np.eye(N), (1, 2, N, N)).copy()
+    for causal in (False, True):
+        o, _ = attn(q, k, v, causal, 0.4)
+        assert np.all(o >= 0)
+        np.testing.assert_allclose(o.sum(axis=-1), 1.0, rtol=0, atol=1e-12)
+        if causal:
+            upper = np.triu(np.ones((N, N), dtype=bool), 1)
+            assert np.all(o[..., upper] == 0)
+            assert np.all(o[..., ~upper] > 0)
+
+
+def check_key_permutation(attn):
+    """Non-causal attention is invariant to permuting keys and values together."""
+    B, H, N, d = 1, 2, 50, 8
+    q, k, v = (_rand((B, H, N, d), s) for s in (14, 15, 16))
+    perm = _rng(17).permutation(N)
+    o1, l1 = attn(q, k, v, False, 0.35)
+    o2, l2 = attn(q, k[:, :, perm], v[:, :, perm], False, 0.35)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-12)
+
+
+def check_logit_shift(attn):
+    """Adding a constant a_i to every logit of row i leaves O unchanged and adds
+    a_i to lse.  The shift is built by appending one feature: q' = [q, a/scale],
+    k' = [k, 1] (and a zero column to V, dropped again)."""
+    B, H, N, d = 1, 1, 29, 6
+    q, k, v = (_rand((B, H, N, d), s) for s in (18, 19, 20))
+    scale = 0.45
+    a = _rand((B, H, N), 21, 5.0)
+    q2 = np.concatenate([q, (a / scale)[..., None]], axis=-1)
+    k2 = np.concatenate([k, np.ones((B, H, N, 1))], axis=-1)
+    v2 = np.concatenate([v, np.zeros((B, H, N, 1))], axis=-1)
+    for causal in (False, True):
+        o1, l1 = attn(q, k, v, causal, scale)
+        o2, l2 = attn(q2, k2, v2, causal, scale)
+        np.testing.assert_allclose(o2[..., :d], o1, rtol=0, atol=1e-11)
+        np.testing.assert_allclose(l2, l1 + a, rtol=0, atol=1e-11)
+
+
+def check_orthogonal_invariance(attn):
+    """Q M and K M with M orthogonal give the same logits, hence the same O, lse."""
+    B, H, N, d = 1, 2, 40, 16
+    q, k, v = (_rand((B, H, N, d), s) for s in (22, 23, 24))
+    m, _ = np.linalg.qr(_rand((d, d), 25))
+    for causal in (False, True):
+        o1, l1 = attn(q, k, v, causal, 0.25)
+        o2, l2 = attn(q @ m, k @ m, v, causal, 0.25)
+        np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-11)
+        np.testing.assert_allclose(l2, l1, rtol=0, atol=1e-11)
+
+
+def brute_force(q, k, v, causal, scale):
+    """Row by row in pure Python: weights exp(s) with no max subtraction
+    (inputs keep |s| small), normalised by their plain sum."""
+    B, H, N, d = q.shape
+    o = np.zeros((B, H, N, d))
+    lse = np.zeros((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            for i in range(N):
+                keys = range(i + 1) if causal else range(N)
+                weights = []
+                for j in keys:
+                    s = scale * sum(float(q[b, h, i, c]) * float(k[b, h, j, c]) for c in range(d))
+                    weights.append(math.exp(s))
+                total = sum(weights)
+                for c in range(d):
+                    o[b, h, i, c] = sum(w * float(v[b, h, j, c]) for w, j in zip(weights, keys)) / total
+                lse[b, h, i] = math.log(total)
+    return o, lse
+
+
+def check_brute_force(attn):
+    """Tiny non-square cases (N != d) against the pure-Python evaluation."""
+    for (B, H, N, d), seed in (((1, 1, 1, 1), 30), ((1, 2, 7, 3), 31), ((2, 1, 16, 8), 32),
+                               ((1, 1, 11, 5), 33)):
+        q, k, v = (_rand((B, H, N, d), seed + 100 * s) for s in range(3))
+        scale = 0.9 / math.sqrt(d)
+        for causal in (False, True):
+            o, lse = attn(q, k, v, causal, scale)
+            ob, lb = brute_force(q, k, v, causal, scale)
+            np.testing.assert_allclose(o, ob, rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse, lb, rtol=0, atol=1e-12)
+
+
+def check_golden(attn):
+    """Hand-worked examples with exact expected values."""
+    with open(os.path.join(GOLDEN, "two_key_softmax.json")) as f:
+        cases = json.load(f)["cases"]
+    for case in cases:
+        q = np.array(case["q"], dtype=np.float64)[None, None]
+        k = np.array(case["k"], dtype=np.float64)[None, None]
+        v = np.array(case["v"], dtype=np.float64)[None, None]
+        o, lse = attn(q, k, v, case["causal"], case["scale"])
+        rows = case["rows_checked"]
+        np.testing.assert_allclose(o[0, 0, rows], np.array(case["o"]), rtol=0, atol=1e-12,
+                                   err_msg=case["name"])
+        np.testing.assert_allclose(lse[0, 0, rows], np.array(case["lse"]), rtol=0, atol=1e-12,
+                                   err_msg=case["name"])
+
+
+def check_row_subset(attn):
+    """Rows computed on their own equal the same rows of the full computation."""
+    B, H, N, d = 1, 2, 31, 8
+    q, k, v = (_rand((B, H, N, d), s) for s in (40, 41, 42))
+    rows = np.array([0, 3, 17, 30])
+    for causal in (False, True):
+        o, lse = attn(q, k, v, causal, 0.3)
+        os_, ls_ = attn(q, k, v, causal, 0.3, rows=rows)
+        np.testing.assert_array_equal(os_, o[:, :, rows])
+        np.testing.assert_array_equal(ls_, lse[:, :, rows])
+
+
+ALL_CHECKS = [check_zero_query_is_mean, check_zero_scale_is_mean, check_causal_row0,
+              check_constant_v, check_weights_are_probabilities, check_key_permutation,
+              check_logit_shift, check_orthogonal_invariance, check_brute_force,
+              check_golden, check_row_subset]

@@ -1,0 +1,50 @@
+"""Plausible mistakes planted in copies of the oracle must each fail a pin.
+
+Each mutant is the oracle's C source with one textual change (a dropped term,
+a wrong sign, a wrong index or operand), compiled by gcc into a temporary
+library and checked in a child process, so the real oracle is never touched."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.c")
+
+MUTANTS = [
+    ("dropped scale", "w[j] = J->scale * dot;", "w[j] = dot;"),
+    ("causal mask off by one", "J->causal ? i + 1 : J->N", "J->causal ? i : J->N"),
+    ("value used as key", "qi[c] * kh[j * J->d + c]", "qi[c] * vh[j * J->d + c]"),
+    ("sign of exponent", "w[j] = exp(w[j] - m);", "w[j] = exp(m - w[j]);"),
+    ("missing normalisation", "oi[c] /= l;", "oi[c] /= 1.0;"),
+    ("lse without max", "m + log(l)", "log(l)"),
+    ("max not subtracted", "w[j] = exp(w[j] - m);", "w[j] = exp(w[j]);"),
+    ("subset row index", "(bh * J->N + i) * J->d", "(bh * J->N + r) * J->d"),
+    ("values from head 0", "J->v + bh * J->N * J->d", "J->v + 0 * J->N * J->d"),
+    ("one key dropped", "for (int64_t j = 0; j < nkeys; ++j)\n            for (int64_t c = 0; c < J->d; ++c) oi[c] +=",
+     "for (int64_t j = 1; j < nkeys; ++j)\n            for (int64_t c = 0; c < J->d; ++c) oi[c] +="),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_fails_a_pin(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site not found once: {old!r}"
+    path = tmp_path / "mutant.c"
+    path.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread", "-D_GNU_SOURCE",
+                    str(path), "-o", str(lib), "-lm"], check=True)
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "tests", "_mutant_runner.py"), str(lib)],
+                         capture_output=True, text=True, timeout=300)
+    assert res.returncode == 1, f"mutant '{name}' survived every pin: {res.stdout}{res.stderr}"
+
+
+def test_unmutated_copy_passes_every_pin(tmp_path):
+    lib = tmp_path / "libcopy.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread", "-D_GNU_SOURCE",
+                    SRC, "-o", str(lib), "-lm"], check=True)
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "tests", "_mutant_runner.py"), str(lib)],
+                         capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stdout + res.stderr
