@@ -1,0 +1,196 @@
+"""GB300 (sm_103a) exact attention forward -- Python binding of the C ABI.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``_build/libattn_gb300.so`` (declared in ``include/attn.h``).
+PyTorch supplies device memory and streams.  There is no fallback: if the
+library is missing or a call fails, an exception is raised.
+
+The operation is exact attention, O = softmax(scale * Q K^T [+ causal mask]) V
+with the per-row logsumexp ("FlashAttention -- one, two, three!", section
+"Standard Attention"), computed by one fused tiled kernel.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+import threading
+
+import torch
+
+from . import build as _build
+
+__all__ = ["attn_fwd", "attn_fwd_host", "host_workspace_bytes", "device_status",
+           "set_wait_timeout_ns", "debug_bounded_wait", "status_string", "library_path",
+           "AttnError", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
+           "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "exported_symbols"]
+
+ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_MISALIGNED, ATTN_ERR_CUDA, \
+    ATTN_ERR_TIMEOUT = range(6)
+ATTN_FP16, ATTN_BF16 = 0, 1
+_DTYPES = {torch.float16: ATTN_FP16, torch.bfloat16: ATTN_BF16}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is not built; run __graft_entry__.build() "
+                                   "(the CUDA library is required, there is no fallback)")
+            lib = ctypes.CDLL(path)
+            vp, i32, f32, u64, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float,
+                                     ctypes.c_uint64, ctypes.c_size_t)
+            lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp]
+            lib.attn_fwd.restype = i32
+            lib.attn_fwd_host_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+            lib.attn_fwd_host_workspace_bytes.restype = sz
+            lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32,
+                                          vp, sz, vp]
+            lib.attn_fwd_host.restype = i32
+            lib.attn_get_device_status.argtypes = [vp]
+            lib.attn_get_device_status.restype = i32
+            lib.attn_set_wait_timeout_ns.argtypes = [u64]
+            lib.attn_set_wait_timeout_ns.restype = None
+            lib.attn_debug_bounded_wait.argtypes = [u64, vp]
+            lib.attn_debug_bounded_wait.restype = i32
+            lib.attn_last_cuda_error.argtypes = []
+            lib.attn_last_cuda_error.restype = i32
+            lib.attn_status_string.argtypes = [i32]
+            lib.attn_status_string.restype = ctypes.c_char_p
+            lib.attn_version.argtypes = []
+            lib.attn_version.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def lib():
+    """The loaded ctypes library (raises if it is not built)."""
+    return _load()
+
+
+def exported_symbols():
+    """Names of the functions ``include/attn.h`` declares."""
+    hdr = os.path.join(os.path.dirname(_build.PKG), "include", "attn.h")
+    text = open(hdr).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+
+
+def status_string(status: int) -> str:
+    return _load().attn_status_string(int(status)).decode()
+
+
+def _stream_handle(stream, device) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(st: int, what: str):
+    if st != ATTN_OK:
+        raise AttnError(st, what)
+
+
+def _shape_of(q, k, v):
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must share one [B, H, N, d] shape")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in _DTYPES:
+        raise ValueError("q, k, v must all be float16 or all bfloat16")
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous [B, H, N, d]")
+    return tuple(int(s) for s in q.shape)
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+             scale: float | None = None, out: torch.Tensor | None = None,
+             lse: torch.Tensor | None = None, return_lse: bool = True, stream=None):
+    """Exact attention forward on CUDA tensors [B, H, N, d] (fp16 or bf16).
+
+    Returns (O, lse) with O like q and lse float32 [B, H, N] (None when
+    ``return_lse`` is false and no ``lse`` buffer is given).
+    """
+    B, H, N, d = _shape_of(q, k, v)
+    if not (q.is_cuda and k.device == q.device and v.device == q.device):
+        raise ValueError("q, k, v must be CUDA tensors on one device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous()
+                            or tuple(lse.shape) != (B, H, N)):
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    with torch.cuda.device(q.device):
+        st = _load().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              None if lse is None else lse.data_ptr(), B, H, N, d,
+                              int(bool(causal)), float(scale), _DTYPES[q.dtype],
+                              _stream_handle(stream, q.device))
+    _check(st, "attn_fwd")
+    return out, lse
+
+
+def host_workspace_bytes(B: int, H: int, N: int, d: int, dtype=torch.bfloat16) -> int:
+    return int(_load().attn_fwd_host_workspace_bytes(B, H, N, d, _DTYPES[dtype]))
+
+
+def attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                  scale: float | None = None, workspace: torch.Tensor | None = None,
+                  out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                  device=None, stream=None):
+    """The same operation on host tensors (pinned memory recommended): the
+    library copies the inputs to ``workspace`` on the device, runs the kernel
+    and copies O and lse back, synchronising the stream before it returns."""
+    B, H, N, d = _shape_of(q, k, v)
+    if q.is_cuda:
+        raise ValueError("attn_fwd_host takes host tensors")
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = host_workspace_bytes(B, H, N, d, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    if out is None:
+        out = torch.empty_like(q, pin_memory=q.is_pinned())
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=q.is_pinned())
+    with torch.cuda.device(device):
+        st = _load().attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                   lse.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
+                                   _DTYPES[q.dtype], workspace.data_ptr(), workspace.numel(),
+                                   _stream_handle(stream, device))
+    _check(st, "attn_fwd_host")
+    return out, lse
+
+
+def device_status(stream=None) -> int:
+    """Synchronise ``stream``; return and clear the device status word."""
+    dev = torch.cuda.current_device()
+    return int(_load().attn_get_device_status(_stream_handle(stream, dev)))
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    _load().attn_set_wait_timeout_ns(int(ns))
+
+
+def debug_bounded_wait(timeout_ns: int, stream=None) -> None:
+    dev = torch.cuda.current_device()
+    _check(_load().attn_debug_bounded_wait(int(timeout_ns), _stream_handle(stream, dev)),
+           "attn_debug_bounded_wait")

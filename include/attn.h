@@ -1,0 +1,135 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) exact attention forward library.
+ *
+ * The operation is exact softmax attention, computed by one fused tiled kernel
+ * that never writes the N x N score matrix to memory:
+ *
+ *   O   = softmax(scale * Q K^T  [+ causal mask]) V
+ *   lse = per-row log-sum-exp of the scaled (masked) logits, natural log
+ *
+ * Definition: "FlashAttention -- one, two, three!", section "Standard
+ * Attention" (the three-pass computation whose result is reproduced exactly),
+ * and sections "FlashAttention v1." (tiling, running denominator, a few
+ * per-row constants kept in global memory) and "FlashAttention v2." (deferred
+ * normalisation, parallelism over batch, heads and sequence).  The FP8 entry
+ * points follow "Incoherent Processing for FP8 Accuracy" (FlashAttention-3
+ * podcast page) and item 3 of "Метод" in the comrad404 review (block
+ * quantisation plus a random-sign Hadamard rotation of Q and K).
+ *
+ * Conventions shared by every entry point:
+ *  - Layout: Q, K, V, O are contiguous [B, H, N, d] (row-major, d innermost);
+ *    self-attention, so queries and keys share N.  lse is contiguous [B, H, N].
+ *  - Device pointers are CUDA device addresses on the current device; every
+ *    tensor base must be 16-byte aligned (lse: 4-byte aligned).
+ *  - Ownership: the caller owns every buffer.  The library never allocates
+ *    device memory; it keeps one device status word per kernel module.
+ *  - Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  All
+ *    device-pointer entry points are asynchronous on that stream.
+ *  - Errors: arguments are validated before anything is launched; a bad
+ *    argument returns a status code and launches nothing.  Nothing throws
+ *    across this boundary.  A kernel whose internal wait runs past its time
+ *    limit stops cleanly and records ATTN_ERR_TIMEOUT in the device status
+ *    word, read with attn_get_device_status().
+ *  - Causal mask: query i sees keys j <= i (queries and keys aligned at 0).
+ *    Keys beyond N never contribute; rows beyond N are never written.
+ */
+#ifndef GB300_ATTN_H
+#define GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* NULL pointer, non-positive size, non-finite scale, ... */
+  ATTN_ERR_UNSUPPORTED = 2, /* head dim or dtype this build has no kernel for */
+  ATTN_ERR_MISALIGNED = 3,  /* a base pointer breaks the alignment rule above */
+  ATTN_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed (see attn_last_cuda_error) */
+  ATTN_ERR_TIMEOUT = 5      /* a kernel wait ran past its limit (device status word) */
+} attn_status;
+
+typedef enum { ATTN_FP16 = 0, ATTN_BF16 = 1 } attn_dtype;
+
+/*
+ * attn_fwd -- exact attention forward, 16-bit inputs and output.
+ *
+ *   q, k, v : [B, H, N, d] device, dtype `dtype` (fp16 or bf16), read only.
+ *   o       : [B, H, N, d] device, same dtype, written (rounded to nearest even).
+ *   lse     : [B, H, N] device float32, written; may be NULL (not written).
+ *   B, H, N : >= 0 each; when B*H*N == 0 nothing is launched and ATTN_OK returned.
+ *   d       : head dimension, one of 64, 128, 256.
+ *   causal  : 0 = full attention, 1 = causal mask.
+ *   scale   : multiplies Q K^T before the softmax; any finite value (0 allowed).
+ *   stream  : cudaStream_t.
+ *
+ * Accumulation is float32 on the tensor cores; the softmax weights P are
+ * rounded to the input dtype before the P V product, and O is normalised once
+ * at the end.  Returns ATTN_OK once the kernel is enqueued.
+ */
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                     int N, int d, int causal, float scale, attn_dtype dtype, void* stream);
+
+/*
+ * attn_fwd_host_workspace_bytes -- device workspace (bytes) attn_fwd_host needs
+ * for these sizes: room for Q, K, V, O and lse, each 256-byte aligned.
+ */
+size_t attn_fwd_host_workspace_bytes(int B, int H, int N, int d, attn_dtype dtype);
+
+/*
+ * attn_fwd_host -- the same operation on HOST buffers.
+ *
+ *   q_host, k_host, v_host : [B, H, N, d] host memory (pinned memory makes the
+ *                            copies asynchronous and fast), read only.
+ *   o_host                 : [B, H, N, d] host, written.
+ *   lse_host               : [B, H, N] host float32, written; may be NULL.
+ *   workspace              : device buffer of at least
+ *                            attn_fwd_host_workspace_bytes(...) bytes, 256-byte
+ *                            aligned, owned by the caller.
+ * Copies the inputs host->device on `stream`, runs attn_fwd, copies O (and lse)
+ * back, and synchronises `stream` before returning.
+ */
+attn_status attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host,
+                          float* lse_host, int B, int H, int N, int d, int causal, float scale,
+                          attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_get_device_status -- synchronises `stream`, then returns and clears the
+ * device status word of every kernel module: ATTN_ERR_TIMEOUT if any kernel
+ * recorded a timed-out wait since the last call, else ATTN_OK (ATTN_ERR_CUDA if
+ * the synchronisation itself failed).
+ */
+attn_status attn_get_device_status(void* stream);
+
+/*
+ * attn_set_wait_timeout_ns -- limit for every internal wait of later launches
+ * (default 1e9 ns).  0 restores the default.  Process-wide.
+ */
+void attn_set_wait_timeout_ns(uint64_t timeout_ns);
+
+/*
+ * attn_debug_bounded_wait -- launches one tiny kernel that waits on a barrier
+ * nothing ever signals, using the same bounded wait as the attention kernels,
+ * with limit `timeout_ns`.  It exists so that the timeout path can be tested
+ * without hanging a GPU: afterwards attn_get_device_status() reports
+ * ATTN_ERR_TIMEOUT.  Asynchronous on `stream`.
+ */
+attn_status attn_debug_bounded_wait(uint64_t timeout_ns, void* stream);
+
+/* Last CUDA error code seen by the library (cudaError_t as int; 0 = none). */
+int attn_last_cuda_error(void);
+
+/* Human-readable name of a status code (static storage). */
+const char* attn_status_string(attn_status status);
+
+/* Library version, e.g. "0.1.0". */
+const char* attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_ATTN_H */

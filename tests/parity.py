@@ -1,0 +1,61 @@
+"""Element-by-element comparison of the CUDA path with the float64 oracle.
+
+Tolerances for 16-bit inputs: max |dO| <= 1e-2, RMS(dO) <= 2e-3, max |dlse| <=
+1e-3 (absolute).  Both sides read the same rounded inputs, so the only
+differences are the kernel's float32 accumulation, its 16-bit rounding of the
+softmax weights P and of O.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import exact_attention_forward_05_gb300 as attn
+import oracle
+import synth
+
+MAX_ABS, RMS, LSE_ABS = 1e-2, 2e-3, 1e-3
+
+
+def metrics(o_gpu, lse_gpu, o_ref, lse_ref):
+    o = o_gpu.double().cpu().numpy() if hasattr(o_gpu, "cpu") else np.asarray(o_gpu, np.float64)
+    l = lse_gpu.double().cpu().numpy() if hasattr(lse_gpu, "cpu") else np.asarray(lse_gpu, np.float64)
+    d = o - o_ref
+    return {"max_abs": float(np.abs(d).max()) if d.size else 0.0,
+            "rms": float(np.sqrt(np.mean(d ** 2))) if d.size else 0.0,
+            "lse_abs": float(np.abs(l - lse_ref).max()) if l.size else 0.0,
+            "finite": bool(np.isfinite(o).all() and np.isfinite(l).all())}
+
+
+def assert_close(m, what=""):
+    assert m["finite"], f"{what}: non-finite output"
+    assert m["max_abs"] <= MAX_ABS, f"{what}: max |dO| {m['max_abs']:.3e} > {MAX_ABS}"
+    assert m["rms"] <= RMS, f"{what}: RMS {m['rms']:.3e} > {RMS}"
+    assert m["lse_abs"] <= LSE_ABS, f"{what}: max |dlse| {m['lse_abs']:.3e} > {LSE_ABS}"
+
+
+def run_gpu(q, k, v, causal, scale, device="cuda"):
+    o, lse = attn.attn_fwd(q.to(device), k.to(device), v.to(device), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def check_case(q, k, v, causal, scale=None, rows=None, what=""):
+    """Run the kernel, compare every output row (or the sampled ``rows``) with
+    the oracle; returns the metrics."""
+    d = q.shape[-1]
+    scale = d ** -0.5 if scale is None else scale
+    o, lse = run_gpu(q, k, v, causal, scale)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=causal, scale=scale, rows=rows)
+    if rows is not None:
+        idx = torch.as_tensor(rows, device=o.device)
+        o, lse = o[:, :, idx], lse[:, :, idx]
+    m = metrics(o, lse, o_ref, lse_ref)
+    assert_close(m, what)
+    st = attn.device_status()
+    assert st == attn.ATTN_OK, f"{what}: device status {attn.status_string(st)}"
+    return m
+
+
+def inputs(B, H, N, d, dtype="bf16", seed=0):
+    return synth.attention_inputs(B, H, N, d, dtype, seed)

@@ -1,0 +1,82 @@
+"""The C-ABI library: builds, loads, exports every declared symbol, and rejects
+bad arguments before any CUDA work (no GPU needed)."""
+import ctypes
+
+import pytest
+
+import exact_attention_forward_05_gb300 as attn
+from exact_attention_forward_05_gb300 import build as attn_build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    attn_build.build()
+    return attn.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = attn.exported_symbols()
+    assert "attn_fwd" in names and "attn_fwd_host" in names
+    raw = ctypes.CDLL(attn.library_path())
+    missing = [n for n in names if not hasattr(raw, n)]
+    assert not missing, f"declared in include/attn.h but not exported: {missing}"
+
+
+def test_status_strings_and_version(lib):
+    assert attn.status_string(attn.ATTN_OK) == "ATTN_OK"
+    assert attn.status_string(attn.ATTN_ERR_TIMEOUT) == "ATTN_ERR_TIMEOUT"
+    assert attn.status_string(99) == "ATTN_ERR_UNKNOWN"
+    assert lib.attn_version().decode().count(".") == 2
+
+
+def _fwd(lib, q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, B=1, H=1, N=8, d=128,
+         causal=0, scale=0.1, dtype=attn.ATTN_BF16):
+    # Fake, never-dereferenced addresses: validation runs before any CUDA call.
+    return lib.attn_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, None)
+
+
+def test_validation_before_launch(lib):
+    assert _fwd(lib, d=96) == attn.ATTN_ERR_UNSUPPORTED
+    assert _fwd(lib, d=32) == attn.ATTN_ERR_UNSUPPORTED
+    assert _fwd(lib, dtype=7) == attn.ATTN_ERR_UNSUPPORTED
+    assert _fwd(lib, q=None) == attn.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, o=None) == attn.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, N=-1) == attn.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, B=-3) == attn.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, scale=float("nan")) == attn.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, scale=float("inf")) == attn.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, q=0x1008) == attn.ATTN_ERR_MISALIGNED
+    assert _fwd(lib, v=0x3002) == attn.ATTN_ERR_MISALIGNED
+    assert _fwd(lib, lse=0x5002) == attn.ATTN_ERR_MISALIGNED
+    assert _fwd(lib, B=65536, H=65536) == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_empty_problem_launches_nothing(lib):
+    # B*H*N == 0 is a valid no-op: ATTN_OK without touching CUDA or the pointers.
+    assert _fwd(lib, N=0, q=None, k=None, v=None, o=None) == attn.ATTN_OK
+    assert _fwd(lib, B=0) == attn.ATTN_OK
+    assert _fwd(lib, H=0, lse=None) == attn.ATTN_OK
+
+
+def test_host_workspace_size(lib):
+    n = attn.host_workspace_bytes(2, 3, 100, 64)
+    elems = 2 * 3 * 100 * 64
+    up = lambda x: (x + 255) // 256 * 256
+    assert n == 4 * up(elems * 2) + up(2 * 3 * 100 * 4)
+    assert lib.attn_fwd_host(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 1, 1, 8, 128, 0, 0.1,
+                             attn.ATTN_BF16, None, 0, None) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_host(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 1, 1, 8, 128, 0, 0.1,
+                             attn.ATTN_BF16, 0x10000, 16, None) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_host(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 1, 1, 8, 128, 0, 0.1,
+                             attn.ATTN_BF16, 0x10010, 1 << 20, None) == attn.ATTN_ERR_MISALIGNED
+
+
+def test_python_wrapper_rejects_bad_tensors(lib):
+    import torch
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        attn.attn_fwd(q, q, q.float())
+    with pytest.raises(ValueError):
+        attn.attn_fwd(q, q, q[:, :, :4])
+    with pytest.raises(ValueError):
+        attn.attn_fwd(q, q, q)  # host tensors: the device path needs CUDA tensors

@@ -1,0 +1,139 @@
+"""GPU parity: the CUDA kernel against the float64 oracle, element by element,
+on seeded inputs that span several tiles, ragged tails and the edge cases."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_forward_05_gb300 as attn
+import oracle
+import synth
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tiny_fp16_config():
+    """fp16, B=1, H=2, N=256, d=64, scale 1/sqrt(d), iid N(0,1) from seed 0."""
+    q, k, v = parity.inputs(1, 2, 256, 64, "fp16", seed=0)
+    for causal in (False, True):
+        parity.check_case(q, k, v, causal, what=f"tiny fp16 causal={causal}")
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("N", [1, 7, 128, 129, 255, 300, 640])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_sizes_bf16(d, N, causal):
+    q, k, v = parity.inputs(2, 3, N, d, "bf16", seed=N * 7 + d)
+    parity.check_case(q, k, v, causal, what=f"bf16 d={d} N={N} causal={causal}")
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_fp16(d, causal):
+    q, k, v = parity.inputs(1, 2, 383, d, "fp16", seed=11 + d)
+    parity.check_case(q, k, v, causal, what=f"fp16 d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_b4_h16_n2048_d128(causal):
+    """bf16, B=4, H=16, N=2048, d=128, every row checked (512 units: several
+    persistent rounds per CTA)."""
+    q, k, v = parity.inputs(4, 16, 2048, 128, "bf16", seed=0)
+    parity.check_case(q, k, v, causal, what=f"B4 H16 N2048 causal={causal}")
+
+
+def test_single_head_many_blocks():
+    q, k, v = parity.inputs(1, 1, 4099, 128, "bf16", seed=3)
+    for causal in (False, True):
+        parity.check_case(q, k, v, causal, what=f"BH=1 N=4099 causal={causal}")
+
+
+def test_zero_scale_is_uniform_average():
+    q, k, v = parity.inputs(1, 2, 300, 128, "bf16", seed=4)
+    for causal in (False, True):
+        parity.check_case(q, k, v, causal, scale=0.0, what=f"scale 0 causal={causal}")
+
+
+def test_negative_scale():
+    q, k, v = parity.inputs(1, 2, 257, 64, "bf16", seed=5)
+    for causal in (False, True):
+        parity.check_case(q, k, v, causal, scale=-0.2, what=f"negative scale causal={causal}")
+
+
+def test_zero_query_gives_mean():
+    _, k, v = parity.inputs(1, 2, 200, 64, "bf16", seed=6)
+    q = torch.zeros_like(k)
+    o, lse = parity.run_gpu(q, k, v, False, 0.125)
+    want = v.double().mean(dim=2, keepdim=True).expand_as(v)
+    assert (o.double().cpu() - want).abs().max().item() <= 1e-2
+    assert (lse.double().cpu() - math.log(200)).abs().max().item() <= 1e-3
+
+
+def test_growing_logits_exercise_rescale():
+    """Logits that grow by about 11.5 (log2 units) per key block force the
+    running maximum up in every block, so O is rescaled every block."""
+    B, H, N, d = 1, 2, 1024, 64
+    q = torch.zeros(B, H, N, d)
+    q[..., 0] = 1.0
+    k = torch.randn(B, H, N, d, generator=torch.Generator().manual_seed(7)) * 0.1
+    k[..., 0] = torch.arange(N, dtype=torch.float32) / 16.0
+    v = torch.randn(B, H, N, d, generator=torch.Generator().manual_seed(8))
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    for causal in (False, True):
+        parity.check_case(q, k, v, causal, scale=1.0, what=f"growing logits causal={causal}")
+
+
+def test_large_magnitude_logits():
+    """scale * |q| * |k| around 100: exercises max subtraction at large range."""
+    q, k, v = parity.inputs(1, 2, 777, 128, "bf16", seed=9)
+    q = (q.float() * 3).to(torch.bfloat16)
+    k = (k.float() * 3).to(torch.bfloat16)
+    for causal in (False, True):
+        parity.check_case(q, k, v, causal, scale=1.0, what=f"large logits causal={causal}")
+
+
+def test_preallocated_outputs_stream_and_no_lse():
+    q, k, v = (t.cuda() for t in parity.inputs(2, 2, 333, 128, "bf16", seed=10))
+    out = torch.full_like(q, float("nan"))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o, lse = attn.attn_fwd(q, k, v, causal=True, out=out, return_lse=False, stream=s)
+    s.synchronize()
+    assert lse is None and o.data_ptr() == out.data_ptr()
+    o_ref, _ = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True)
+    assert np.abs(o.double().cpu().numpy() - o_ref).max() <= 1e-2
+
+
+def test_misaligned_device_pointer_is_rejected():
+    q, k, v = (t.cuda() for t in parity.inputs(1, 1, 65, 64, "bf16", seed=12))
+    flat = torch.empty(q.numel() + 8, dtype=q.dtype, device="cuda")
+    shifted = flat[1:1 + q.numel()].view_as(q)  # 2-byte offset
+    shifted.copy_(q)
+    with pytest.raises(attn.AttnError) as e:
+        attn.attn_fwd(shifted, k, v)
+    assert e.value.status == attn.ATTN_ERR_MISALIGNED
+
+
+def test_empty_inputs():
+    for shape in [(0, 2, 16, 64), (1, 0, 16, 64), (1, 2, 0, 64)]:
+        q = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+        o, lse = attn.attn_fwd(q, q, q)
+        assert o.shape == q.shape and lse.shape == shape[:3]
+
+
+def test_host_buffer_entry_point():
+    q, k, v = (t.pin_memory() for t in parity.inputs(2, 4, 520, 128, "bf16", seed=13))
+    for causal in (False, True):
+        o, lse = attn.attn_fwd_host(q, k, v, causal=causal)
+        o_ref, lse_ref = oracle.attention(q, k, v, causal=causal)
+        parity.assert_close(parity.metrics(o, lse, o_ref, lse_ref), f"host path causal={causal}")
+
+
+def test_repeated_calls_are_deterministic():
+    q, k, v = (t.cuda() for t in parity.inputs(2, 8, 1000, 128, "bf16", seed=14))
+    o1, l1 = attn.attn_fwd(q, k, v, causal=True)
+    o2, l2 = attn.attn_fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
