@@ -1,0 +1,393 @@
+"""Benchmark of the exact attention forward on GB300.
+
+Default workload: the sequence-length sweep point N = 8192, d = 128 (bf16,
+B = 16384 / N = 2, H = 2048 / d = 16, non-causal; the causal run of the same
+shapes is reported beside it).  A step is one launch of the fused attention
+kernel over that batch.  Metric: attention forward TFLOP/s with
+FLOPs = 4 B H N^2 d (halved when causal), and its fraction of the measured
+dense BF16 tensor peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the float64 CPU oracle, host cores
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(weak scaling: the path has no exchange step); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s and % of GB300 dense BF16/FP8 tensor peak vs seq len"
+UNIT = "TFLOP/s"
+FALLBACK_BF16_TFLOPS = 1900.0
+KERNEL_SOURCE = os.path.join(ROOT, "exact_attention_forward_05_gb300", "csrc", "attn_fwd.cu")
+PROFILE_JSON = os.path.join(ROOT, "profiles", "attn_fwd_bf16_b2_h16_n8192_d128.json")
+
+WORKLOADS = {}
+for _n in (512, 1024, 2048, 4096, 8192, 16384):
+    for _d in (64, 128, 256):
+        for _c in (False, True):
+            WORKLOADS[f"sweep_n{_n}_d{_d}{'_causal' if _c else ''}"] = dict(
+                B=16384 // _n, H=2048 // _d, N=_n, d=_d, causal=_c, dtype="bf16")
+WORKLOADS["b4_h16_n2048_d128"] = dict(B=4, H=16, N=2048, d=128, causal=False, dtype="bf16")
+WORKLOADS["b4_h16_n2048_d128_causal"] = dict(B=4, H=16, N=2048, d=128, causal=True, dtype="bf16")
+WORKLOADS["long_b1_h16_n32768_d128_causal"] = dict(B=1, H=16, N=32768, d=128, causal=True, dtype="bf16")
+DEFAULT_WORKLOAD = "sweep_n8192_d128"
+
+
+def flops(w) -> float:
+    f = 4.0 * w["B"] * w["H"] * w["N"] ** 2 * w["d"]
+    return f / 2 if w["causal"] else f
+
+
+def describe(w) -> str:
+    return (f"{w['dtype']} attention fwd, B={w['B']}, H={w['H']}, N={w['N']}, d={w['d']}, "
+            f"{'causal' if w['causal'] else 'non-causal'}")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    return FALLBACK_BF16_TFLOPS, "fallback (1.9 PFLOP/s bf16 burst, one earlier GB300 measurement)"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) with host timestamps."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            ident = str(device_index)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={ident}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], [], set()
+        for ts, f in self.samples:
+            if not (t0 <= ts <= t1) or len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- GPU arm
+
+def time_kernel(fn, steps: int, warmup: int, stream):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev[0].record(stream)
+    for _ in range(steps):
+        fn()
+    ev[1].record(stream)
+    torch.cuda.synchronize()
+    return ev[0].elapsed_time(ev[1])  # ms
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def traffic_from_profile():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source."""
+    if not os.path.exists(PROFILE_JSON):
+        return None
+    with open(PROFILE_JSON) as f:
+        prof = json.load(f)
+    sha = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()
+    if prof.get("kernel_source_sha256") != sha:
+        return None
+    return prof.get("dram_bytes_per_launch_full_workload")
+
+
+def sampled_parity(o, lse, q, k, v, w, rows):
+    import oracle  # test infrastructure: parity check outside the timed region
+    o_ref, lse_ref = oracle.attention(q[:1, :1], k[:1, :1], v[:1, :1], causal=w["causal"],
+                                      scale=w["d"] ** -0.5, rows=rows)
+    idx = torch.as_tensor(rows)
+    og = o[:1, :1, idx].double().cpu().numpy()
+    lg = lse[:1, :1, idx].double().cpu().numpy()
+    return {"rows": len(rows), "max_abs": float(np.abs(og - o_ref).max()),
+            "lse_abs": float(np.abs(lg - lse_ref).max())}
+
+
+def cpu_baseline(w, q, k, v, budget_s: float = 12.0):
+    """The oracle as it stands, on every host core, on a bounded sample of the
+    workload: whole heads (all their query rows) when one head fits the time
+    budget, else seeded query rows of one head; throughput in TFLOP/s."""
+    import oracle
+    import synth
+    B, H, N, d = w["B"], w["H"], w["N"], w["d"]
+    qf, kf, vf = (t.reshape(1, B * H, N, d) for t in (q, k, v))
+    scale = d ** -0.5
+    probe = synth.sample_rows(N, 64, seed=1, salt=99)
+    t0 = time.time()
+    oracle.attention(qf[:, :1], kf[:, :1], vf[:, :1], causal=w["causal"], scale=scale, rows=probe)
+    t_head = max(time.time() - t0, 1e-4) * N / len(probe)
+    if t_head <= budget_s:
+        nh = int(min(B * H, max(1, budget_s // t_head)))
+        rows = None
+        keys = nh * (N * (N + 1) // 2 if w["causal"] else N * N)
+        what = f"{nh} of {B * H} heads, all {N} query rows each"
+    else:
+        nh = 1
+        rows = synth.sample_rows(N, int(max(16, N * budget_s / t_head)), seed=2, salt=98)
+        keys = int((rows + 1).sum()) if w["causal"] else len(rows) * N
+        what = f"{len(rows)} seeded query rows of head 0"
+    t0 = time.time()
+    _, _, used = oracle.attention(qf[:, :nh], kf[:, :nh], vf[:, :nh], causal=w["causal"],
+                                  scale=scale, rows=rows, return_threads=True)
+    dt = time.time() - t0
+    fl = 4.0 * float(keys) * d
+    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": f"{what} (float64 C oracle, {dt:.1f} s)", "seconds": dt}
+
+
+def run_gpu(args):
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import exact_attention_forward_05_gb300 as attn
+    import synth
+
+    w = WORKLOADS[args.workload]
+    B, H, N, d = w["B"], w["H"], w["N"], w["d"]
+    q, k, v = synth.attention_inputs(B, H, N, d, w["dtype"], seed=rank)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    scale = d ** -0.5
+    launches = [0]
+
+    def step(causal=w["causal"]):
+        attn.attn_fwd(qd, kd, vd, causal=causal, scale=scale, out=o, lse=lse, stream=stream)
+        launches[0] += 1
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(1.0 if sampler else 0.0)
+    barrier(world)
+    # warm-up, then exactly `steps` timed launches between barriers
+    for _ in range(args.warmup):
+        step()
+    barrier(world)
+    launches[0] = 0
+    t_wall0 = time.time()
+    ms = time_kernel(step, args.steps, 0, stream)
+    t_wall1 = time.time()
+    barrier(world)
+    n_launch = launches[0]
+    ms_max = max_over_ranks(ms, world)
+    status = attn.device_status()
+    if status != attn.ATTN_OK:
+        raise RuntimeError(f"device status {attn.status_string(status)}")
+    per_step = ms_max / args.steps
+    value = flops(w) * world / (per_step * 1e-3) / 1e12
+
+    # the other mask setting of the same shapes, for context
+    other = dict(w, causal=not w["causal"])
+    ms_o = max_over_ranks(time_kernel(lambda: step(other["causal"]), max(args.steps // 4, 3), 3,
+                                      stream), world)
+    other_value = flops(other) * world / (ms_o / max(args.steps // 4, 3) * 1e-3) / 1e12
+    step()  # leave o / lse for the configured mask
+    torch.cuda.synchronize()
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    if sampler:
+        sampler.stop()
+
+    # end to end: host buffers (pinned) through the C ABI, copies in the timed region
+    qp, kp, vp = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    op = torch.empty_like(qp).pin_memory()
+    lp = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    ws = torch.empty(attn.host_workspace_bytes(B, H, N, d, qd.dtype), dtype=torch.uint8, device=dev)
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        attn.attn_fwd_host(qp, kp, vp, causal=w["causal"], scale=scale, workspace=ws, out=op,
+                           lse=lp, device=dev)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        attn.attn_fwd_host(qp, kp, vp, causal=w["causal"], scale=scale, workspace=ws, out=op,
+                           lse=lp, device=dev)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world) / e2e_steps
+    e2e_value = flops(w) * world / e2e_s / 1e12
+
+    peak, peak_src = peaks()
+    achieved = flops(w) / (ms / args.steps * 1e-3) / 1e12
+    line = None
+    if rank == 0:
+        rows = synth.sample_rows(N, 16, seed=0, salt=7)
+        par = sampled_parity(o.cpu(), lse.cpu(), q, k, v, w, rows)
+        cpu = cpu_baseline(w, q, k, v)
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w["dtype"], "data": "synthetic (seeded iid N(0,1), splitmix64 + Box-Muller)",
+            "config": {"workload": describe(w), "B": B, "H": H, "N": N, "d": d,
+                       "causal": w["causal"], "scale": scale,
+                       "flops_per_step_per_gpu": flops(w),
+                       "l2": "inputs larger than L2 (Q, K, V, O = 4 x %.0f MiB)" % (B * H * N * d * 2 / 2 ** 20),
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                         "peak_source": peak_src, "traffic": traffic_from_profile(),
+                         "kernel": "attn_fwd_kernel<128, bf16>"},
+            "cpu_baseline": {k2: (round(v2, 6) if isinstance(v2, float) else v2)
+                             for k2, v2 in cpu.items() if k2 != "seconds"},
+            "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
+                    "h2d_bytes_per_step": 3 * q.numel() * q.element_size(),
+                    "d2h_bytes_per_step": o.numel() * o.element_size() + lse.numel() * 4,
+                    "path": "attn_fwd_host (pinned host buffers)"},
+            "gpu_launches": n_launch,
+            "clocks": clocks,
+            "other_mask": {"causal": other["causal"], "value": round(other_value, 2), "unit": UNIT},
+            "parity_sample": par,
+            "device": torch.cuda.get_device_name(dev),
+        }
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return line
+
+
+# --------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    import synth
+    w = WORKLOADS[args.workload]
+    N, d = w["N"], w["d"]
+    # The oracle needs only the rows it computes plus the keys and values of head 0.
+    q, k, v = synth.attention_inputs(1, 1, N, d, w["dtype"], seed=0)
+    probe = synth.sample_rows(N, 16, seed=3, salt=97)
+    t0 = time.time()
+    _, _, used = oracle.attention(q, k, v, causal=w["causal"], scale=d ** -0.5, rows=probe,
+                                  return_threads=True)
+    per_row = max(time.time() - t0, 1e-4) / len(probe)
+    budget = 90.0  # seconds for the whole run
+    rows_per_step = int(max(1, min(N, budget / (args.steps + args.warmup) / per_row)))
+    total_fl, total_t = 0.0, 0.0
+    for i in range(args.warmup + args.steps):
+        rows = synth.sample_rows(N, rows_per_step, seed=4 + i, salt=96)
+        t0 = time.time()
+        oracle.attention(q, k, v, causal=w["causal"], scale=d ** -0.5, rows=rows)
+        dt = time.time() - t0
+        if i >= args.warmup:
+            keys = (rows + 1).sum() if w["causal"] else len(rows) * N
+            total_fl += 4.0 * float(keys) * d
+            total_t += dt
+    value = total_fl / total_t / 1e12
+    sample = (f"{rows_per_step} query rows of one head per step (all their keys), float64, "
+              f"{args.steps} timed steps")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total_t / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded iid N(0,1))",
+            "config": {"workload": describe(w), "B": w["B"], "H": w["H"], "N": N, "d": d,
+                       "causal": w["causal"], "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    line = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -40,9 +40,28 @@ def run_gpu(q, k, v, causal, scale, device="cuda"):
     return o, lse
 
 
-def check_case(q, k, v, causal, scale=None, rows=None, what=""):
+# Unit roundoff of the 16-bit formats (significand bits incl. the hidden bit: 8, 11).
+UNIT_ROUNDOFF = {torch.bfloat16: 2.0 ** -8, torch.float16: 2.0 ** -11}
+
+
+def assert_within_rounding(o_gpu, o_ref, v, what=""):
+    """Bound for outputs of any magnitude, derived from the arithmetic: O is
+    rounded once to the 16-bit format (relative error <= u |O|) and every
+    softmax weight once (|dO| <= u max|v| since the weights sum to one), plus
+    the 1e-2 float32 accumulation allowance."""
+    u = UNIT_ROUNDOFF[o_gpu.dtype]
+    o = o_gpu.double().cpu().numpy()
+    vmax = float(v.double().abs().max())
+    bound = MAX_ABS + u * (np.abs(o_ref) + vmax)
+    excess = np.abs(o - o_ref) - bound
+    assert np.all(excess <= 0), f"{what}: exceeds the rounding bound by {excess.max():.3e}"
+
+
+def check_case(q, k, v, causal, scale=None, rows=None, what="", large_outputs=False):
     """Run the kernel, compare every output row (or the sampled ``rows``) with
-    the oracle; returns the metrics."""
+    the oracle; returns the metrics.  ``large_outputs`` replaces the fixed
+    max-abs bound by the rounding bound above (for inputs whose outputs reach
+    several units, where one bf16 ulp alone exceeds 1e-2)."""
     d = q.shape[-1]
     scale = d ** -0.5 if scale is None else scale
     o, lse = run_gpu(q, k, v, causal, scale)
@@ -51,6 +70,9 @@ def check_case(q, k, v, causal, scale=None, rows=None, what=""):
         idx = torch.as_tensor(rows, device=o.device)
         o, lse = o[:, :, idx], lse[:, :, idx]
     m = metrics(o, lse, o_ref, lse_ref)
+    if large_outputs:
+        assert_within_rounding(o, o_ref, v, what)
+        m = dict(m, max_abs=0.0)
     assert_close(m, what)
     st = attn.device_status()
     assert st == attn.ATTN_OK, f"{what}: device status {attn.status_string(st)}"

@@ -86,12 +86,15 @@ def test_growing_logits_exercise_rescale():
 
 
 def test_large_magnitude_logits():
-    """scale * |q| * |k| around 100: exercises max subtraction at large range."""
+    """scale * |q| * |k| around 100: exercises max subtraction at large range.
+    The softmax is nearly one-hot, so |O| reaches max|V| (about 4.5) and the
+    bf16 rounding of O alone can exceed 1e-2: checked against the rounding bound."""
     q, k, v = parity.inputs(1, 2, 777, 128, "bf16", seed=9)
     q = (q.float() * 3).to(torch.bfloat16)
     k = (k.float() * 3).to(torch.bfloat16)
     for causal in (False, True):
-        parity.check_case(q, k, v, causal, scale=1.0, what=f"large logits causal={causal}")
+        parity.check_case(q, k, v, causal, scale=1.0, what=f"large logits causal={causal}",
+                          large_outputs=True)
 
 
 def test_preallocated_outputs_stream_and_no_lse():
