@@ -21,7 +21,7 @@ import torch
 
 from . import build as _build
 
-__all__ = ["attn_fwd", "attn_fwd_host", "host_workspace_bytes", "device_status",
+__all__ = ["attn_fwd", "attn_fwd_host", "fp8_prepare", "attn_fwd_fp8", "attn_fwd_fp8_pipeline", "host_workspace_bytes", "device_status",
            "set_wait_timeout_ns", "debug_bounded_wait", "status_string", "library_path",
            "AttnError", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
            "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "exported_symbols"]
@@ -63,6 +63,12 @@ def _load():
             lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32,
                                           vp, sz, vp]
             lib.attn_fwd_host.restype = i32
+            lib.attn_fp8_prepare.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, i32,
+                                             i32, i32, i32, i32, vp]
+            lib.attn_fp8_prepare.restype = i32
+            lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
+                                         i32, f32, vp]
+            lib.attn_fwd_fp8.restype = i32
             lib.attn_get_device_status.argtypes = [vp]
             lib.attn_get_device_status.restype = i32
             lib.attn_set_wait_timeout_ns.argtypes = [u64]
@@ -178,6 +184,70 @@ def attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: boo
                                    _stream_handle(stream, device))
     _check(st, "attn_fwd_host")
     return out, lse
+
+
+FP8_BLOCK = 128  # rows per quantisation scale block
+
+
+def fp8_prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, signs: torch.Tensor | None = None,
+                per_tensor: bool = False, stream=None):
+    """FP8 pre-pass on CUDA tensors [B, H, N, 128] (fp16 or bf16): random-sign
+    Hadamard rotation of Q and K (when ``signs`` [H, 128] int8 is given) and
+    E4M3 quantisation with one float32 scale per 128 rows of a head (or one per
+    tensor).  Returns (q8, k8, v8, q_scale, k_scale, v_scale); the codes are
+    uint8 tensors [B, H, N, 128]."""
+    B, H, N, d = _shape_of(q, k, v)
+    if not q.is_cuda:
+        raise ValueError("fp8_prepare takes CUDA tensors")
+    nblk = (N + FP8_BLOCK - 1) // FP8_BLOCK
+    codes = [torch.empty((B, H, N, d), dtype=torch.uint8, device=q.device) for _ in range(3)]
+    sshape = (1,) if per_tensor else (B, H, nblk)
+    scales = [torch.empty(sshape, dtype=torch.float32, device=q.device) for _ in range(3)]
+    if signs is not None:
+        if signs.dtype != torch.int8 or tuple(signs.shape) != (H, d):
+            raise ValueError("signs must be an int8 [H, d] tensor of +1 / -1")
+        signs = signs.to(q.device).contiguous()
+    with torch.cuda.device(q.device):
+        st = _load().attn_fp8_prepare(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), _DTYPES[q.dtype],
+            *(c.data_ptr() for c in codes), *(sc.data_ptr() for sc in scales),
+            None if signs is None else signs.data_ptr(), int(bool(per_tensor)), B, H, N, d,
+            _stream_handle(stream, q.device))
+    _check(st, "attn_fp8_prepare")
+    return (*codes, *scales)
+
+
+def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False,
+                 scale: float | None = None, out: torch.Tensor | None = None,
+                 lse: torch.Tensor | None = None, return_lse: bool = True, stream=None):
+    """Exact attention on E4M3 codes (uint8 [B, H, N, 128]) and float32 scales
+    (per block [B, H, ceil(N/128)] or per tensor [1]); bf16 output."""
+    if q8.dim() != 4 or q8.shape != k8.shape or q8.shape != v8.shape:
+        raise ValueError("q8, k8, v8 must share one [B, H, N, d] shape")
+    B, H, N, d = (int(s_) for s_ in q8.shape)
+    per_tensor = q_scale.numel() == 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    with torch.cuda.device(q8.device):
+        st = _load().attn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), q_scale.data_ptr(),
+                                  k_scale.data_ptr(), v_scale.data_ptr(), int(per_tensor),
+                                  out.data_ptr(), None if lse is None else lse.data_ptr(),
+                                  B, H, N, d, int(bool(causal)), float(scale),
+                                  _stream_handle(stream, q8.device))
+    _check(st, "attn_fwd_fp8")
+    return out, lse
+
+
+def attn_fwd_fp8_pipeline(q, k, v, signs=None, causal: bool = False, scale: float | None = None,
+                          per_tensor: bool = False, stream=None):
+    """fp8_prepare followed by attn_fwd_fp8 (the quantised operands are
+    allocated here, as torch tensors)."""
+    q8, k8, v8, qs, ks, vs = fp8_prepare(q, k, v, signs=signs, per_tensor=per_tensor, stream=stream)
+    return attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=causal, scale=scale, stream=stream)
 
 
 def device_status(stream=None) -> int:

@@ -1,15 +1,233 @@
-// attn_fp8.cu -- FP8 (E4M3) path: pre-pass and attention kernel.
-#include "host_common.h"
+// attn_fp8.cu -- FP8 (E4M3) path of the exact attention forward.
+//
+// Pre-pass ("Incoherent Processing for FP8 Accuracy", FlashAttention-3 podcast
+// page; comrad404 review, "Метод", item 3): every row of Q and K is multiplied
+// by diag(sigma_h) H_128 / sqrt(128) -- random signs of its head, then the
+// Sylvester Hadamard transform, O(d log d) butterflies -- and Q, K, V are
+// quantised to E4M3 with one float32 scale per 128 rows of a head:
+// s = amax / 448 (1 when the block is all zero), code = RNE_satfinite(x / s).
+// The rotation is orthogonal and shared by Q and K of a head, so Q K^T is
+// unchanged; V is not rotated.  A per-tensor mode (one scale per tensor, no
+// rotation) gives the naive FP8 baseline the pages compare against.
+//
+// The attention kernel itself is attn_kernel::attn_fwd_kernel<128, E4M3>.
+#include "attn_kernel.cuh"
+
+using attn_kernel::FwdParams;
+using attn_kernel::KIND_E4M3;
 
 namespace {
-__device__ unsigned int g_status_fp8 = 0;
+
+constexpr int kHeadDim = 128;     // FP8 path: d = 128
+constexpr int kQuantRows = 128;   // rows per scale block
+constexpr int kPrepThreads = 256; // 8 warps x 16 rows each
+constexpr float kE4M3Max = 448.0f;
+
+enum PrepMode : int { PREP_BLOCK = 0, PREP_AMAX = 1, PREP_QUANT_GLOBAL = 2 };
+
+struct PrepParams {
+  const void* src[3];
+  uint8_t* dst[3];
+  float* scale[3];
+  const int8_t* signs;  // [H][128] +-1, or nullptr (no rotation)
+  int H, N, nblk;
+};
+
+// Sylvester-ordered fast Walsh-Hadamard transform of one 128-element row held
+// as 4 consecutive elements per lane (element 4*lane + e): butterflies of
+// stride 1 and 2 inside the thread, strides 4..64 across lanes.
+__device__ __forceinline__ void fwht128(float (&x)[4], int lane) {
+  const float a0 = x[0] + x[1], a1 = x[0] - x[1], a2 = x[2] + x[3], a3 = x[2] - x[3];
+  x[0] = a0 + a2;
+  x[2] = a0 - a2;
+  x[1] = a1 + a3;
+  x[3] = a1 - a3;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float o = __shfl_xor_sync(0xffffffffu, x[e], m);
+      x[e] = upper ? (o - x[e]) : (x[e] + o);
+    }
+  }
+}
+
+template <bool BF16IN, int MODE>
+__global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const PrepParams p) {
+  const int t = blockIdx.y;                     // 0 = Q, 1 = K, 2 = V
+  const int blk = blockIdx.x % p.nblk;
+  const int bh = blockIdx.x / p.nblk;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool rotate = t < 2 && p.signs != nullptr;
+  const size_t head = static_cast<size_t>(bh) * p.N * kHeadDim;
+  const uint8_t* src = static_cast<const uint8_t*>(p.src[t]);
+
+  float x[16][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int row = blk * kQuantRows + warp + 8 * i;
+    if (row < p.N) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(src + (head + static_cast<size_t>(row) * kHeadDim + 4 * lane) * 2);
+      if constexpr (BF16IN) {
+        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+        x[i][0] = f0.x; x[i][1] = f0.y; x[i][2] = f1.x; x[i][3] = f1.y;
+      } else {
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+        x[i][0] = f0.x; x[i][1] = f0.y; x[i][2] = f1.x; x[i][3] = f1.y;
+      }
+    } else {
+      x[i][0] = x[i][1] = x[i][2] = x[i][3] = 0.f;
+    }
+  }
+  if (rotate) {
+    const int8_t* sg = p.signs + (bh % p.H) * kHeadDim + 4 * lane;
+    const float s0 = sg[0], s1 = sg[1], s2 = sg[2], s3 = sg[3];
+    const float inv_sqrt_d = 0.08838834764831845f;  // 1 / sqrt(128)
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      x[i][0] *= s0; x[i][1] *= s1; x[i][2] *= s2; x[i][3] *= s3;
+      fwht128(x[i], lane);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[i][e] *= inv_sqrt_d;
+    }
+  }
+
+  // amax of the block
+  __shared__ float warp_max[kPrepThreads / 32];
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) a = fmaxf(a, fabsf(x[i][e]));
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
+  if (lane == 0) warp_max[warp] = a;
+  __syncthreads();
+  float amax = 0.f;
+#pragma unroll
+  for (int w = 0; w < kPrepThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
+
+  if constexpr (MODE == PREP_AMAX) {
+    if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned int*>(p.scale[t]), __float_as_uint(amax));
+    return;
+  } else {
+    float s;
+    if constexpr (MODE == PREP_BLOCK) {
+      s = amax > 0.f ? amax / kE4M3Max : 1.f;
+      if (threadIdx.x == 0) p.scale[t][static_cast<size_t>(bh) * p.nblk + blk] = s;
+    } else {
+      const float g = __uint_as_float(*reinterpret_cast<const unsigned int*>(p.scale[t]));
+      s = g > 0.f ? g / kE4M3Max : 1.f;
+    }
+    uint8_t* dst = p.dst[t];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int row = blk * kQuantRows + warp + 8 * i;
+      if (row >= p.N) continue;
+      const uint32_t lo = __nv_cvt_float2_to_fp8x2(
+          make_float2(__fdiv_rn(x[i][0], s), __fdiv_rn(x[i][1], s)), __NV_SATFINITE, __NV_E4M3);
+      const uint32_t hi = __nv_cvt_float2_to_fp8x2(
+          make_float2(__fdiv_rn(x[i][2], s), __fdiv_rn(x[i][3], s)), __NV_SATFINITE, __NV_E4M3);
+      *reinterpret_cast<uint32_t*>(dst + head + static_cast<size_t>(row) * kHeadDim + 4 * lane) = lo | (hi << 16);
+    }
+  }
+}
+
+// Per-tensor mode: the scale slot held the tensor amax (as bits); turn it into s.
+__global__ void fp8_finalize_scale_kernel(float* q_scale, float* k_scale, float* v_scale) {
+  float* sc[3] = {q_scale, k_scale, v_scale};
+  if (threadIdx.x < 3) {
+    const float g = __uint_as_float(*reinterpret_cast<unsigned int*>(sc[threadIdx.x]));
+    *sc[threadIdx.x] = g > 0.f ? g / kE4M3Max : 1.f;
+  }
+}
+
+template <bool BF16IN>
+attn_status run_prepare(const PrepParams& prm, int BH, int per_tensor, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>(BH) * prm.nblk, 3);
+  if (!per_tensor) {
+    fp8_prepare_kernel<BF16IN, PREP_BLOCK><<<grid, kPrepThreads, 0, s>>>(prm);
+    return attn_internal::cuda_status(cudaGetLastError());
+  }
+  for (int t = 0; t < 3; ++t) {
+    cudaError_t e = cudaMemsetAsync(prm.scale[t], 0, sizeof(float), s);
+    if (e != cudaSuccess) return attn_internal::cuda_status(e);
+  }
+  fp8_prepare_kernel<BF16IN, PREP_AMAX><<<grid, kPrepThreads, 0, s>>>(prm);
+  fp8_prepare_kernel<BF16IN, PREP_QUANT_GLOBAL><<<grid, kPrepThreads, 0, s>>>(prm);
+  fp8_finalize_scale_kernel<<<1, 32, 0, s>>>(prm.scale[0], prm.scale[1], prm.scale[2]);
+  return attn_internal::cuda_status(cudaGetLastError());
+}
+
+attn_status check_common(int B, int H, int N, int d) {
+  if (B < 0 || H < 0 || N < 0) return ATTN_ERR_INVALID_ARG;
+  if (d != kHeadDim) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * H > 0x7fffffff / 64) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
 }  // namespace
 
 namespace attn_internal {
-cudaError_t fp8_status_exchange(unsigned int* out) {
-  cudaError_t e = cudaMemcpyFromSymbol(out, g_status_fp8, sizeof(unsigned int));
-  if (e != cudaSuccess) return e;
-  const unsigned int zero = 0;
-  return cudaMemcpyToSymbol(g_status_fp8, &zero, sizeof(unsigned int));
-}
+cudaError_t fp8_status_exchange(unsigned int* out) { return attn_kernel::status_exchange(out); }
 }  // namespace attn_internal
+
+ATTN_EXPORT attn_status attn_fp8_prepare(const void* q, const void* k, const void* v, attn_dtype in_dtype,
+                                         void* q8, void* k8, void* v8, float* q_scale, float* k_scale,
+                                         float* v_scale, const int8_t* signs, int per_tensor, int B,
+                                         int H, int N, int d, void* stream) {
+  attn_status st = check_common(B, H, N, d);
+  if (st != ATTN_OK) return st;
+  if (in_dtype != ATTN_FP16 && in_dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * H * N == 0) return ATTN_OK;
+  if (!q || !k || !v || !q8 || !k8 || !v8 || !q_scale || !k_scale || !v_scale) return ATTN_ERR_INVALID_ARG;
+  using attn_internal::aligned;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(q8, 16) || !aligned(k8, 16) ||
+      !aligned(v8, 16))
+    return ATTN_ERR_MISALIGNED;
+  if (!aligned(q_scale, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4)) return ATTN_ERR_MISALIGNED;
+  PrepParams prm;
+  prm.src[0] = q; prm.src[1] = k; prm.src[2] = v;
+  prm.dst[0] = static_cast<uint8_t*>(q8);
+  prm.dst[1] = static_cast<uint8_t*>(k8);
+  prm.dst[2] = static_cast<uint8_t*>(v8);
+  prm.scale[0] = q_scale; prm.scale[1] = k_scale; prm.scale[2] = v_scale;
+  prm.signs = signs;
+  prm.H = H;
+  prm.N = N;
+  prm.nblk = (N + kQuantRows - 1) / kQuantRows;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int BH = B * H;
+  return in_dtype == ATTN_BF16 ? run_prepare<true>(prm, BH, per_tensor, s)
+                               : run_prepare<false>(prm, BH, per_tensor, s);
+}
+
+ATTN_EXPORT attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale,
+                                     const float* k_scale, const float* v_scale, int per_tensor, void* o,
+                                     float* lse, int B, int H, int N, int d, int causal, float scale,
+                                     void* stream) {
+  attn_status st = check_common(B, H, N, d);
+  if (st != ATTN_OK) return st;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(B) * H * N == 0) return ATTN_OK;
+  if (!q8 || !k8 || !v8 || !o || !q_scale || !k_scale || !v_scale) return ATTN_ERR_INVALID_ARG;
+  using attn_internal::aligned;
+  if (!aligned(q8, 16) || !aligned(k8, 16) || !aligned(v8, 16) || !aligned(o, 16)) return ATTN_ERR_MISALIGNED;
+  if (!aligned(q_scale, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4)) return ATTN_ERR_MISALIGNED;
+  if (lse && !aligned(lse, 4)) return ATTN_ERR_MISALIGNED;
+  FwdParams prm{};
+  prm.o = o;
+  prm.lse = lse;
+  prm.causal = causal ? 1 : 0;
+  prm.q_scale = q_scale;
+  prm.k_scale = k_scale;
+  prm.v_scale = v_scale;
+  const int nblk = (N + kQuantRows - 1) / kQuantRows;
+  prm.scale_bh_stride = per_tensor ? 0 : nblk;
+  prm.scale_blk_stride = per_tensor ? 0 : 1;
+  return attn_kernel::launch_fwd<kHeadDim, KIND_E4M3>(q8, k8, v8, prm, B, H, N, scale,
+                                                      static_cast<cudaStream_t>(stream));
+}

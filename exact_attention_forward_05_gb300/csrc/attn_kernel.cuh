@@ -1,0 +1,663 @@
+// attn_kernel.cuh -- the fused exact attention forward kernel for GB300
+// (sm_103a), templated on the head dimension and on the operand kind
+// (fp16, bf16, or FP8 E4M3 with per-block scales).
+//
+// One persistent CTA per SM walks a static list of work units.  A unit is one
+// (batch*head, block of query rows) pair: two 128-row Q tiles for d <= 128,
+// one for d = 256.  Inside a CTA the warps specialise:
+//
+//   softmax group t (4 warps per Q tile): thread = one query row = one TMEM
+//       lane.  Loads its row of S from TMEM, runs the online softmax, writes P
+//       back over S, rescales O when needed, and at the end divides O by the
+//       running sum and stores O and lse.
+//   load warp: TMA loads of Q (once per unit) and of K_j / V_j blocks into a
+//       ring of shared-memory stages guarded by mbarriers.
+//   MMA warp: one thread issues tcgen05.mma: S = Q K_j^T (both operands in
+//       shared memory) and O += P V_j (P read from TMEM, V from shared memory),
+//       accumulating in TMEM, and signals completion with tcgen05.commit.
+//
+// The pages' method: tiles of Q, K, V moved to on-chip memory, the softmax
+// computed blockwise with a running maximum and a separately tracked running
+// denominator, the normalisation deferred to the end ("FlashAttention -- one,
+// two, three!", sections "FlashAttention v1." and "FlashAttention v2."), the
+// softmax of one tile overlapped with the matrix products of another, and
+// asynchronous copies overlapped with compute ("Overlapping GEMM and Softmax
+// (Asynchrony)" on the FlashAttention-3 podcast page; comrad404 review,
+// "Метод", items 1 and 2).  The Hopper ping-pong between two warpgroups is
+// re-expressed for tcgen05: the single MMA issuer alternates between the two Q
+// tiles, so one tile's softmax runs while the other tile's products run.
+//
+// Online softmax, base 2 with c = scale * log2(e):
+//   m_blk = c * rowmax(S_j)           (rowmin when c < 0)
+//   if m_blk > m + 8: O *= 2^(m - m_blk), l *= 2^(m - m_blk), m = m_blk
+//   P_j = 2^(c S_j - m),  l += rowsum(P_j),  O += P_j V_j
+//   O /= l at the end,  lse = (m + log2 l) * ln 2.
+// Keeping a stale m while the block maximum stays within 2^8 of it is exact:
+// O and l carry the same factor 2^-m, which cancels in O / l and is added back
+// in lse; P stays below 2^8, far from overflow in any operand format.
+//
+// FP8 operands (block quantisation, comrad404 review "Метод" item 3): the
+// kernel reads E4M3 codes and float32 scales, one per 128 rows of a head.  The
+// true logit is scale * sq * sk_j * (Q8 K8_j^T), so the per-block multiplier
+// c_j = c * sq * sk_j replaces c.  The V block scale enters through P: the
+// stored weights are P'_j = P_j * sv_j / svmax (svmax = the largest V scale of
+// the head, so P' <= P), l still sums P_j, and O is multiplied by svmax at
+// the end.  In real arithmetic this is the same result; only the rounding
+// point of P moves.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include <cmath>
+
+#include "host_common.h"
+#include "sm103.cuh"
+
+namespace attn_kernel {
+
+using namespace sm103;
+
+// Each translation unit that includes this header owns one status word.
+namespace {
+__device__ unsigned int g_status_word = 0;
+}
+
+enum Kind : int { KIND_F16 = 0, KIND_BF16 = 1, KIND_E4M3 = 2 };
+
+constexpr int kBM = 128;  // query rows per Q tile (= TMEM lanes)
+constexpr int kBN = 128;  // keys per K/V block
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D, int KIND>
+struct Cfg {
+  static constexpr int ELEM = KIND == KIND_E4M3 ? 1 : 2;  // operand bytes
+  static constexpr int NQ = D <= 128 ? 2 : 1;              // Q tiles per unit
+  static constexpr int ROW_BYTES = D * ELEM;
+  static constexpr int CHUNK_BYTES = kBM * 128;  // 128 rows x one 128-byte swizzle span
+  static constexpr int CHUNK_ELEMS = 128 / ELEM;
+  static constexpr int CHUNKS = ROW_BYTES / 128;
+  static constexpr int TILE_BYTES = CHUNKS * CHUNK_BYTES;
+  static constexpr int KSTEP = 32 / ELEM;       // K elements per MMA instruction
+  static constexpr int QK_STEPS = D / KSTEP;
+  static constexpr int PV_STEPS = kBN / KSTEP;
+  static constexpr int P_COLS = kBN * ELEM / 4;  // TMEM columns holding one row of P
+  static constexpr int STAGES = KIND == KIND_E4M3 ? 8 : (D == 64 ? 6 : (D == 128 ? 4 : 2));
+  static constexpr int SOFTMAX_WARPS = 4 * NQ;
+  static constexpr int LOAD_WARP = SOFTMAX_WARPS;
+  static constexpr int MMA_WARP = SOFTMAX_WARPS + 1;
+  static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 2);
+  // TMEM columns: two S buffers, then the O accumulator(s).
+  static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D;
+  static constexpr uint32_t TMEM_COLS = 512;
+  // Barrier indices.
+  static constexpr int B_Q_FULL = 0, B_Q_EMPTY = 1, B_KV_FULL = 2, B_KV_EMPTY = 2 + STAGES,
+                       B_S_FULL = 2 + 2 * STAGES, B_P_FULL = B_S_FULL + 2,
+                       B_O_DONE = B_P_FULL + 2, B_MMA_DONE = B_O_DONE + 2, NBARS = B_MMA_DONE + 1;
+  // Shared memory layout (offsets from a 1024-byte aligned base).
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = NQ * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_KV + STAGES * TILE_BYTES;
+  static constexpr int SMEM_BYTES = OFF_BAR + 8 * NBARS + 16 + 1024;
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+  static_assert(SMEM_BYTES > 114 * 1024, "one CTA per SM (TMEM is allocated whole)");
+  static_assert(ROW_BYTES % 128 == 0, "rows span whole 128-byte swizzle spans");
+};
+
+struct FwdParams {
+  void* o;
+  float* lse;
+  int BH, N;
+  int causal;
+  float sl2;  // scale * log2(e)
+  int units_per_head;
+  int num_units;
+  uint64_t timeout_ns;
+  // FP8 only: scales, element (bh, block) at [bh * bh_stride + block * blk_stride].
+  const float* q_scale;
+  const float* k_scale;
+  const float* v_scale;
+  int scale_bh_stride, scale_blk_stride;
+};
+
+struct Unit {
+  int bh, m0, nkb;
+  int nb[2];  // key blocks visited by each Q tile (0 = tile inactive)
+};
+
+// Unit order: causal units longest-first (highest query block first, all heads
+// of one query block together); full attention head-major so that CTAs that
+// run at the same time share K/V through L2.
+template <int NQ>
+__device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
+  Unit w;
+  int qu;
+  if (p.causal) {
+    qu = p.units_per_head - 1 - u / p.BH;
+    w.bh = u % p.BH;
+  } else {
+    w.bh = u / p.units_per_head;
+    qu = u % p.units_per_head;
+  }
+  w.m0 = qu * kBM * NQ;
+  w.nkb = (p.N + kBN - 1) / kBN;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int r0 = w.m0 + kBM * t;
+    if (t >= NQ || r0 >= p.N)
+      w.nb[t] = 0;
+    else
+      w.nb[t] = p.causal ? min(w.nkb, r0 / kBN + 1) : w.nkb;
+  }
+  return w;
+}
+
+// Static persistent schedule, snake order across rounds so that the
+// longest-first causal list spreads evenly over the CTAs.
+__device__ __forceinline__ int unit_of_round(int r, int num_units) {
+  const int G = gridDim.x, c = blockIdx.x;
+  const int u = r * G + ((r & 1) ? (G - 1 - c) : c);
+  return u < num_units ? u : -1;
+}
+
+// Two weights -> one 32-bit TMEM column of 16-bit P (first key in the low half).
+template <int KIND>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (KIND == KIND_F16) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+// Four weights -> one 32-bit TMEM column of E4M3 P (first key in byte 0).
+__device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
+}
+
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
+template <int D, int KIND>
+__global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using C = Cfg<D, KIND>;
+  constexpr int NQ = C::NQ;
+  constexpr bool F8 = KIND == KIND_E4M3;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+
+  const uint32_t sQ = smem_u32(smem + C::OFF_Q);
+  const uint32_t sKV = smem_u32(smem + C::OFF_KV);
+  const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 8 * C::NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+
+  const int warp = static_cast<int>(warp_id());
+  const int lane = static_cast<int>(lane_id());
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(C::B_Q_FULL), 1);
+    mbar_init(BAR(C::B_Q_EMPTY), 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(BAR(C::B_KV_FULL + s), 1);
+      mbar_init(BAR(C::B_KV_EMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(BAR(C::B_S_FULL + b), 1);
+      mbar_init(BAR(C::B_P_FULL + b), 4);
+      mbar_init(BAR(C::B_O_DONE + b), 1);
+    }
+    mbar_init(BAR(C::B_MMA_DONE), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == C::LOAD_WARP && lane == 0) {
+    tma_prefetch(&tmQ);
+    tma_prefetch(&tmK);
+    tma_prefetch(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == C::LOAD_WARP) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const WaitCtx wc{abort_flag, &g_status_word, p.timeout_ns};
+      uint32_t kv_fill = 0, q_iter = 0;
+      bool ok = true;
+      auto load_block = [&](const CUtensorMap* map, int j, int bh) -> bool {
+        const uint32_t s = kv_fill % C::STAGES;
+        const uint32_t ph = (kv_fill / C::STAGES) & 1u;
+        if (!mbar_wait(BAR(C::B_KV_EMPTY + s), ph ^ 1u, wc, attn_internal::kStatusTimeoutLoad))
+          return false;
+        mbar_arrive_expect_tx(BAR(C::B_KV_FULL + s), C::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::CHUNKS; ++c)
+          tma_load_3d(sKV + s * C::TILE_BYTES + c * C::CHUNK_BYTES, map, BAR(C::B_KV_FULL + s),
+                      c * C::CHUNK_ELEMS, j * kBN, bh);
+        ++kv_fill;
+        return true;
+      };
+      for (int r = 0; ok; ++r) {
+        if (r * static_cast<int>(gridDim.x) >= p.num_units) break;
+        const int u = unit_of_round(r, p.num_units);
+        if (u < 0) continue;
+        const Unit w = decode_unit<NQ>(u, p);
+        const int nbmax = max(w.nb[0], w.nb[1]);
+        if (!mbar_wait(BAR(C::B_Q_EMPTY), (q_iter & 1u) ^ 1u, wc, attn_internal::kStatusTimeoutLoad)) {
+          ok = false;
+          break;
+        }
+        ++q_iter;
+        const int nact = (w.nb[0] > 0) + (NQ == 2 && w.nb[1] > 0);
+        mbar_arrive_expect_tx(BAR(C::B_Q_FULL), nact * C::TILE_BYTES);
+        for (int t = 0; t < NQ; ++t) {
+          if (w.nb[t] == 0) continue;
+#pragma unroll
+          for (int c = 0; c < C::CHUNKS; ++c)
+            tma_load_3d(sQ + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmQ, BAR(C::B_Q_FULL),
+                        c * C::CHUNK_ELEMS, w.m0 + kBM * t, w.bh);
+        }
+        // K/V in the order the MMA warp consumes them: K_0, then (K_j, V_{j-1}).
+        for (int j = 0; j <= nbmax && ok; ++j) {
+          if (j < nbmax) ok = load_block(&tmK, j, w.bh);
+          if (ok && j >= 1) ok = load_block(&tmV, j - 1, w.bh);
+        }
+      }
+      // Never leave the CTA with copies in flight: wait for the last fill of
+      // every stage and of Q (already complete on the normal path).
+      for (uint32_t i = 0; i < C::STAGES && i < kv_fill; ++i) {
+        const uint32_t f = kv_fill - 1 - i;
+        mbar_drain(BAR(C::B_KV_FULL + f % C::STAGES), (f / C::STAGES) & 1u, 100000000ull);
+      }
+      if (q_iter > 0) mbar_drain(BAR(C::B_Q_FULL), (q_iter - 1) & 1u, 100000000ull);
+    }
+  } else if (warp == C::MMA_WARP) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const WaitCtx wc{abort_flag, &g_status_word, p.timeout_ns};
+      // kind::f16: 0 = F16, 1 = BF16; kind::f8f6f4: 0 = E4M3.
+      constexpr uint32_t fmt = KIND == KIND_BF16 ? 1u : 0u;
+      constexpr uint32_t IDESC_QK = instr_desc(fmt, fmt, kBM, kBN, 0);
+      constexpr uint32_t IDESC_PV = instr_desc(fmt, fmt, kBM, D, 1);
+      uint32_t kv_use = 0, q_iter = 0;
+      uint32_t pph = 0u;  // bit b: wait parity of P_FULL[b]
+      bool ok = true;
+
+      auto next_stage = [&](uint32_t& slot) -> bool {
+        slot = kv_use % C::STAGES;
+        const uint32_t ph = (kv_use / C::STAGES) & 1u;
+        ++kv_use;
+        if (!mbar_wait(BAR(C::B_KV_FULL + slot), ph, wc, attn_internal::kStatusTimeoutMma)) return false;
+        tc_fence_after();
+        return true;
+      };
+      // S[sbuf] = Q[qt] K^T   (K-major A and B, 128-byte swizzle; 32 bytes of K per MMA)
+      auto issue_qk = [&](int qt, int sbuf, uint32_t kslot) {
+        const uint32_t d_tmem = tmem + (sbuf ? C::TM_S1 : C::TM_S0);
+#pragma unroll
+        for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+          const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+          const uint64_t a = smem_desc_sw128(sQ + qt * C::TILE_BYTES + off, 16, 1024);
+          const uint64_t b = smem_desc_sw128(sKV + kslot * C::TILE_BYTES + off, 16, 1024);
+          mma_ss(d_tmem, a, b, IDESC_QK, kk > 0 ? 1u : 0u, F8);
+        }
+      };
+      // O[ot] (+)= P[sbuf] V   (P from TMEM, V N-major in shared memory; 32 bytes of keys per MMA)
+      auto issue_pv = [&](int ot, int sbuf, uint32_t vslot, bool acc) {
+        const uint32_t d_tmem = tmem + (ot ? C::TM_O1 : C::TM_O0);
+        const uint32_t a_tmem = tmem + (sbuf ? C::TM_S1 : C::TM_S0);
+#pragma unroll
+        for (int kk = 0; kk < C::PV_STEPS; ++kk) {
+          const uint64_t b = smem_desc_sw128(sKV + vslot * C::TILE_BYTES + kk * C::KSTEP * 128,
+                                             C::CHUNK_BYTES, 1024);
+          mma_ts(d_tmem, a_tmem + kk * 8, b, IDESC_PV, (acc || kk > 0) ? 1u : 0u, F8);
+        }
+      };
+      auto wait_p = [&](int b) -> bool {
+        if (!mbar_wait(BAR(C::B_P_FULL + b), (pph >> b) & 1u, wc, attn_internal::kStatusTimeoutMma)) return false;
+        pph ^= 1u << b;
+        tc_fence_after();
+        return true;
+      };
+
+      for (int r = 0; ok; ++r) {
+        if (r * static_cast<int>(gridDim.x) >= p.num_units) break;
+        const int u = unit_of_round(r, p.num_units);
+        if (u < 0) continue;
+        const Unit w = decode_unit<NQ>(u, p);
+        const int nbmax = max(w.nb[0], w.nb[1]);
+        if (!mbar_wait(BAR(C::B_Q_FULL), q_iter & 1u, wc, attn_internal::kStatusTimeoutMma)) { ok = false; break; }
+        ++q_iter;
+        tc_fence_after();
+        uint32_t ks = 0, vs = 0;
+        if constexpr (NQ == 2) {
+          if (!(ok = next_stage(ks))) break;
+          for (int t = 0; t < 2; ++t)
+            if (w.nb[t] > 0) {
+              issue_qk(t, t, ks);
+              mma_commit(BAR(C::B_S_FULL + t));
+            }
+          mma_commit(BAR(C::B_KV_EMPTY + ks));
+          if (nbmax == 1) mma_commit(BAR(C::B_Q_EMPTY));
+          for (int j = 1; j <= nbmax && ok; ++j) {
+            if (j < nbmax && !(ok = next_stage(ks))) break;
+            if (!(ok = next_stage(vs))) break;
+            for (int t = 0; t < 2 && ok; ++t) {
+              if (j - 1 < w.nb[t]) {
+                if (!(ok = wait_p(t))) break;
+                issue_pv(t, t, vs, j - 1 > 0);
+                mma_commit(BAR(C::B_O_DONE + t));
+              }
+              if (j < w.nb[t]) {
+                issue_qk(t, t, ks);
+                mma_commit(BAR(C::B_S_FULL + t));
+              }
+            }
+            if (!ok) break;
+            if (j == nbmax - 1) mma_commit(BAR(C::B_Q_EMPTY));
+            if (j < nbmax) mma_commit(BAR(C::B_KV_EMPTY + ks));
+            mma_commit(BAR(C::B_KV_EMPTY + vs));
+          }
+        } else {
+          const int nb = w.nb[0];
+          if (!(ok = next_stage(ks))) break;
+          issue_qk(0, 0, ks);
+          mma_commit(BAR(C::B_S_FULL + 0));
+          mma_commit(BAR(C::B_KV_EMPTY + ks));
+          if (nb == 1) mma_commit(BAR(C::B_Q_EMPTY));
+          for (int j = 1; j <= nb && ok; ++j) {
+            if (j < nb) {
+              if (!(ok = next_stage(ks))) break;
+              issue_qk(0, j & 1, ks);
+              mma_commit(BAR(C::B_S_FULL + (j & 1)));
+              mma_commit(BAR(C::B_KV_EMPTY + ks));
+              if (j == nb - 1) mma_commit(BAR(C::B_Q_EMPTY));
+            }
+            if (!(ok = next_stage(vs))) break;
+            if (!(ok = wait_p((j - 1) & 1))) break;
+            issue_pv(0, (j - 1) & 1, vs, j - 1 > 0);
+            mma_commit(BAR(C::B_O_DONE + 0));
+            mma_commit(BAR(C::B_KV_EMPTY + vs));
+          }
+        }
+      }
+      // Every MMA issued by this CTA has finished before TMEM is released.
+      mma_commit(BAR(C::B_MMA_DONE));
+      mbar_drain(BAR(C::B_MMA_DONE), 0, 100000000ull);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const WaitCtx wc{abort_flag, &g_status_word, p.timeout_ns};
+    const int wg = warp >> 2;                 // Q tile / O accumulator of this group
+    const int wq = warp & 3;                  // TMEM lane quarter of this warp
+    const int row = wq * 32 + lane;           // row within the Q tile
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t tm_o = lane_base + (wg == 0 ? C::TM_O0 : C::TM_O1);
+    uint32_t sph = 0u, oph = 0u;  // sph bit b: wait parity of S_FULL[b]
+    bool ok = true;
+
+    for (int r = 0; ok; ++r) {
+      if (r * static_cast<int>(gridDim.x) >= p.num_units) break;
+      const int u = unit_of_round(r, p.num_units);
+      if (u < 0) continue;
+      const Unit w = decode_unit<NQ>(u, p);
+      const int nb = w.nb[wg];
+      if (nb == 0) continue;
+      const int tile_row0 = w.m0 + wg * kBM;
+      const int qi = tile_row0 + row;                  // query row of this thread
+      const int diag = tile_row0 / kBN;                // key block holding the diagonal
+      float m_used = -INFINITY, l = 0.f;
+      // FP8: query-block scale and the largest V scale of the blocks visited.
+      float c_q = p.sl2, sv_max = 1.f;
+      if constexpr (F8) {
+        const int sb = w.bh * p.scale_bh_stride;
+        c_q = p.sl2 * p.q_scale[sb + (tile_row0 / kBM) * p.scale_blk_stride];
+        float mx = 0.f;
+        for (int j = 0; j < nb; ++j) mx = fmaxf(mx, p.v_scale[sb + j * p.scale_blk_stride]);
+        sv_max = mx > 0.f ? mx : 1.f;
+      }
+
+      for (int j = 0; j < nb; ++j) {
+        const int b = NQ == 2 ? wg : (j & 1);
+        // Per-block multiplier of S and the V fold (FP8); plain scale otherwise.
+        float cj = c_q, lg2_ratio = 0.f, inv_ratio = 1.f;
+        if constexpr (F8) {
+          const int sb = w.bh * p.scale_bh_stride + j * p.scale_blk_stride;
+          cj = c_q * p.k_scale[sb];
+          const float sv = p.v_scale[sb];
+          if (sv > 0.f && sv < sv_max) {
+            lg2_ratio = log2f(sv / sv_max);
+            inv_ratio = sv_max / sv;
+          }
+        }
+        if (!(ok = mbar_wait_warp(BAR(C::B_S_FULL + b), (sph >> b) & 1u, wc, attn_internal::kStatusTimeoutSoftmax))) break;
+        sph ^= 1u << b;
+        tc_fence_after();
+        const uint32_t tm_s = lane_base + (b ? C::TM_S1 : C::TM_S0);
+
+        uint32_t s[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tm_s + 32 * c, s[c]);
+        tmem_wait_ld(s[0]);
+        reg_pin(s[1]);
+        reg_pin(s[2]);
+        reg_pin(s[3]);
+
+        const bool masked = (p.causal && j == diag) || (j == w.nkb - 1 && (p.N % kBN) != 0);
+        float mblk;
+        if (masked) {
+          // Scale first, then mask: t = c*s for visible keys, -inf otherwise.
+          const int key0 = j * kBN;
+          const int kmax = p.causal ? min(qi, p.N - 1) : p.N - 1;  // last visible key
+          float mx = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float t = (key0 + 32 * c + i <= kmax) ? cj * __uint_as_float(s[c][i]) : -INFINITY;
+              s[c][i] = __float_as_uint(t);
+              mx = fmaxf(mx, t);
+            }
+          mblk = mx;
+        } else {
+          float mx;
+          if (cj >= 0.f) {
+            mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+              for (int i = 0; i < 32; i += 2)
+                mx = max3(mx, __uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1]));
+          } else {
+            mx = INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+              for (int i = 0; i < 32; i += 2)
+                mx = min3(mx, __uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1]));
+          }
+          mblk = cj * mx;
+        }
+
+        float alpha = 1.f;
+        bool rescale = false;
+        if (j == 0) {
+          m_used = (mblk == -INFINITY) ? 0.f : mblk;
+        } else if (mblk > m_used + kRescaleThreshold) {
+          alpha = ex2(m_used - mblk);
+          m_used = mblk;
+          rescale = true;
+        }
+
+        // P = 2^(c*s - m) (FP8: times sv_j / svmax), written over S.
+        float rowsum = 0.f;
+        const float neg_m = lg2_ratio - m_used;
+        if constexpr (!F8) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float x0 = __uint_as_float(s[c][2 * i]), x1 = __uint_as_float(s[c][2 * i + 1]);
+              float p0, p1;
+              if (masked) {
+                p0 = ex2(x0 + neg_m);
+                p1 = ex2(x1 + neg_m);
+              } else {
+                p0 = ex2(fmaf(x0, cj, neg_m));
+                p1 = ex2(fmaf(x1, cj, neg_m));
+              }
+              rowsum += p0 + p1;
+              pk[i] = pack2<KIND>(p0, p1);
+            }
+            tmem_st16(tm_s + 16 * c, pk);
+          }
+        } else {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float pv[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float x = __uint_as_float(s[c][4 * i + e]);
+                pv[e] = masked ? ex2(x + neg_m) : ex2(fmaf(x, cj, neg_m));
+              }
+              rowsum += (pv[0] + pv[1]) + (pv[2] + pv[3]);
+              pk[8 * c + i] = pack4_e4m3(pv[0], pv[1], pv[2], pv[3]);
+            }
+          tmem_st32(tm_s, pk);
+        }
+
+        if (j > 0) {
+          // O holds P_{j-1} V_{j-1} once the previous product has completed.
+          if (!(ok = mbar_wait_warp(BAR(C::B_O_DONE + wg), oph, wc, attn_internal::kStatusTimeoutSoftmax))) break;
+          oph ^= 1u;
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tm_o + 32 * c, o);
+              tmem_wait_ld(o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(tm_o + 32 * c, o);
+            }
+          }
+        }
+        l = l * alpha + rowsum * inv_ratio;
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(C::B_P_FULL + b));
+      }
+      if (!ok) break;
+
+      // Epilogue: O / l (times svmax for FP8), rounded to the output dtype; lse.
+      if (!(ok = mbar_wait_warp(BAR(C::B_O_DONE + wg), oph, wc, attn_internal::kStatusTimeoutSoftmax))) break;
+      oph ^= 1u;
+      tc_fence_after();
+      const float inv_l = sv_max / l;
+      const bool store = qi < p.N;
+      uint8_t* orow = static_cast<uint8_t*>(p.o) +
+                      (static_cast<size_t>(w.bh) * p.N + (store ? qi : 0)) * D * 2;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tm_o + 32 * c, o);
+        tmem_wait_ld(o);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack2<F8 ? KIND_BF16 : KIND>(__uint_as_float(o[2 * i]) * inv_l,
+                                               __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (store) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+      if (store && p.lse != nullptr)
+        p.lse[static_cast<size_t>(w.bh) * p.N + qi] = (m_used + log2f(l)) * 0.69314718055994531f;
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// Host side: encode the three tensor maps, set the shared-memory attribute
+// once per device, and launch one CTA per SM (or per unit, if fewer).
+template <int D, int KIND>
+attn_status launch_fwd(const void* q, const void* k, const void* v, FwdParams prm, int B, int H,
+                       int N, float scale, cudaStream_t stream) {
+  using C = Cfg<D, KIND>;
+  const CUtensorMapDataType dt = KIND == KIND_E4M3   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : KIND == KIND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const uint64_t BH = static_cast<uint64_t>(B) * H;
+  CUtensorMap mq, mk, mv;
+  if (!attn_internal::encode_tmap_3d(&mq, dt, q, D, N, BH, C::ELEM, C::CHUNK_ELEMS, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !attn_internal::encode_tmap_3d(&mk, dt, k, D, N, BH, C::ELEM, C::CHUNK_ELEMS, kBN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !attn_internal::encode_tmap_3d(&mv, dt, v, D, N, BH, C::ELEM, C::CHUNK_ELEMS, kBN, CU_TENSOR_MAP_SWIZZLE_128B))
+    return ATTN_ERR_CUDA;
+
+  static int configured_for[64] = {0};  // per device: dynamic shared memory attribute set
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return attn_internal::cuda_status(e);
+  if (dev >= 64 || !configured_for[dev]) {
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES);
+    if (e != cudaSuccess) return attn_internal::cuda_status(e);
+    if (dev < 64) configured_for[dev] = 1;
+  }
+  prm.BH = static_cast<int>(BH);
+  prm.N = N;
+  prm.sl2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  prm.units_per_head = (N + kBM * C::NQ - 1) / (kBM * C::NQ);
+  prm.num_units = prm.units_per_head * prm.BH;
+  prm.timeout_ns = attn_internal::wait_timeout_ns();
+  const int sms = attn_internal::sm_count();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  const int grid = prm.num_units < sms ? prm.num_units : sms;
+  attn_fwd_kernel<D, KIND><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, prm);
+  return attn_internal::cuda_status(cudaGetLastError());
+}
+
+inline cudaError_t status_exchange(unsigned int* out) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_status_word, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_status_word, &zero, sizeof(unsigned int));
+}
+
+}  // namespace attn_kernel

@@ -97,6 +97,54 @@ attn_status attn_fwd_host(const void* q_host, const void* k_host, const void* v_
                           attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_fp8_prepare -- FP8 pre-pass: incoherent processing and block quantisation
+ * ("Incoherent Processing for FP8 Accuracy", FlashAttention-3 podcast page;
+ * comrad404 review, "Метод", item 3).
+ *
+ *   q, k, v     : [B, H, N, d] device, dtype `in_dtype` (fp16 or bf16), read only.
+ *   q8, k8, v8  : [B, H, N, d] device, E4M3 codes (one byte each), written.
+ *   q_scale, k_scale, v_scale : device float32, written.  Per-block mode:
+ *                 [B, H, ceil(N/128)], one scale per 128 rows of a head.
+ *                 Per-tensor mode: one float each.
+ *   signs       : [H, d] device int8, +1 / -1; NULL = no rotation.  With signs,
+ *                 every row x of Q and K (head h) is replaced by
+ *                 (x * signs[h]) H_d / sqrt(d), H_d the Sylvester Hadamard
+ *                 matrix (an orthogonal map shared by Q and K, so Q K^T is
+ *                 unchanged); V is never rotated.
+ *   per_tensor  : 0 = per-block scales (the FP8 method); 1 = one scale per
+ *                 tensor (the naive FP8 baseline the pages compare against).
+ *   d           : 128 (the FP8 path supports only this head dimension).
+ * Quantisation: s = amax / 448 over the block (or tensor), 1 if amax = 0;
+ * code = E4M3(x / s), division and rounding (nearest even, saturating to
+ * +-448) in float32.  Asynchronous on `stream`.
+ */
+attn_status attn_fp8_prepare(const void* q, const void* k, const void* v, attn_dtype in_dtype,
+                             void* q8, void* k8, void* v8, float* q_scale, float* k_scale,
+                             float* v_scale, const int8_t* signs, int per_tensor, int B, int H,
+                             int N, int d, void* stream);
+
+/*
+ * attn_fwd_fp8 -- exact attention forward on E4M3 operands with float32 scales
+ * (as written by attn_fp8_prepare), bf16 output.
+ *
+ *   q8, k8, v8 : [B, H, N, d] device E4M3 codes, read only; the true values are
+ *                code * scale of their 128-row block (or of the tensor).
+ *   q_scale, k_scale, v_scale : device float32, layout as for attn_fp8_prepare.
+ *   per_tensor : 1 if the scales are single per-tensor values.
+ *   o          : [B, H, N, d] device bf16, written.
+ *   lse        : [B, H, N] device float32 or NULL.
+ *   d          : 128.  Other arguments as for attn_fwd.
+ * Both products run on the FP8 tensor cores with float32 accumulation; the
+ * softmax runs in float32 and P is rounded to E4M3 before P V.  When the
+ * queries and keys were rotated by attn_fp8_prepare, O and lse are those of
+ * the unrotated inputs (up to quantisation).
+ */
+attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale,
+                         const float* k_scale, const float* v_scale, int per_tensor, void* o,
+                         float* lse, int B, int H, int N, int d, int causal, float scale,
+                         void* stream);
+
+/*
  * attn_get_device_status -- synchronises `stream`, then returns and clears the
  * device status word of every kernel module: ATTN_ERR_TIMEOUT if any kernel
  * recorded a timed-out wait since the last call, else ATTN_OK (ATTN_ERR_CUDA if

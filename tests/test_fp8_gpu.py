@@ -1,0 +1,177 @@
+"""FP8 path on the GPU: the pre-pass against the oracle's rotation and block
+quantisation, the FP8 attention kernel against exact attention on the
+dequantised operands, and the end-to-end error against exact attention on the
+16-bit inputs next to the naive per-tensor FP8 baseline."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_forward_05_gb300 as attn
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+D = 128
+FP8_RMS = 2.5e-2     # error bound of the FP8 path against exact attention (target)
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+def _e4m3_step(x):
+    """Spacing of E4M3 values around |x| (2^-9 in the subnormal range)."""
+    a = np.maximum(np.abs(x), 2.0 ** -6)
+    return 2.0 ** (np.floor(np.log2(a)) - 3)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_prepare_without_rotation_is_bit_exact(dtype):
+    """No rotation: both sides divide the same float32 value by the same scale
+    and round to nearest even, so every code and every scale is identical."""
+    q, k, v = synth.outlier_inputs(2, 3, 300, D, dtype, seed=1)
+    out = attn.fp8_prepare(q.cuda(), k.cuda(), v.cuda(), signs=None)
+    torch.cuda.synchronize()
+    for x, c, s in zip((q, k, v), out[:3], out[3:]):
+        codes, scales = oracle.block_quantize(x)
+        np.testing.assert_array_equal(_np(c), codes)
+        np.testing.assert_array_equal(_np(s), scales)
+
+
+def test_prepare_per_tensor_is_bit_exact():
+    q, k, v = synth.outlier_inputs(1, 4, 257, D, "bf16", seed=2)
+    out = attn.fp8_prepare(q.cuda(), k.cuda(), v.cuda(), per_tensor=True)
+    torch.cuda.synchronize()
+    for x, c, s in zip((q, k, v), out[:3], out[3:]):
+        codes, scales = oracle.block_quantize(x, per_tensor=True)
+        assert _np(s).shape == (1,)
+        np.testing.assert_array_equal(_np(s), scales)
+        np.testing.assert_array_equal(_np(c), codes)
+
+
+def test_prepare_with_rotation_matches_oracle():
+    """With the Hadamard rotation the kernel's float32 butterflies and the
+    oracle's float64 dense product round differently, so a code may land on the
+    neighbouring E4M3 value when the quotient sits at a rounding midpoint: the
+    scales agree to float32 rounding, dequantised values to one E4M3 step, and
+    only a small fraction of codes differ.  V is not rotated: bit-exact."""
+    B, H, N = 2, 4, 385
+    q, k, v = synth.outlier_inputs(B, H, N, D, "bf16", seed=3)
+    signs = synth.hadamard_signs(H, D, seed=3)
+    out = attn.fp8_prepare(q.cuda(), k.cuda(), v.cuda(), signs=signs.cuda())
+    torch.cuda.synchronize()
+    for i, x in enumerate((q, k)):
+        rot = oracle.hadamard_rotate(x, signs)
+        codes, scales = oracle.block_quantize(rot)
+        np.testing.assert_allclose(_np(out[3 + i]), scales, rtol=1e-5, atol=0)
+        deq_gpu = oracle.dequantize(_np(out[i]), _np(out[3 + i]))
+        deq_ref = oracle.dequantize(codes, scales)
+        s_rep = np.repeat(scales.astype(np.float64), 128, axis=-1)[..., :N, None]
+        assert np.all(np.abs(deq_gpu - deq_ref) <= _e4m3_step(deq_ref / s_rep) * s_rep * (1 + 1e-6))
+        assert np.mean(_np(out[i]) != codes) < 0.01
+    codes, scales = oracle.block_quantize(v)
+    np.testing.assert_array_equal(_np(out[2]), codes)
+    np.testing.assert_array_equal(_np(out[5]), scales)
+
+
+def test_prepare_rotation_is_orthogonal_on_device():
+    """Dequantised rotated Q and K keep Q K^T: compare the logits of the
+    dequantised codes with those of the 16-bit inputs (up to quantisation)."""
+    q, k, v = synth.attention_inputs(1, 2, 256, D, "bf16", seed=4)
+    signs = synth.hadamard_signs(2, D, seed=4)
+    q8, k8, _, qs, ks, _ = attn.fp8_prepare(q.cuda(), k.cuda(), v.cuda(), signs=signs.cuda())
+    qd = oracle.dequantize(_np(q8), _np(qs))
+    kd = oracle.dequantize(_np(k8), _np(ks))
+    s_fp8 = np.einsum("bhid,bhjd->bhij", qd, kd)
+    s_ref = np.einsum("bhid,bhjd->bhij", q.double().numpy(), k.double().numpy())
+    assert np.sqrt(np.mean((s_fp8 - s_ref) ** 2)) < 0.05 * np.sqrt(np.mean(s_ref ** 2))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [128, 300, 1100])
+def test_fp8_kernel_on_oracle_quantised_operands(N, causal):
+    """The FP8 kernel on operands quantised by the oracle, against exact
+    attention on the dequantised operands.  lse does not depend on the E4M3
+    rounding of P (the running sum adds the float32 weights; the products of
+    two E4M3 codes are exact in float32): 1e-3.  O: the weights are rounded
+    to E4M3 (relative half step 2^-4), so its RMS error is a few percent of
+    the RMS of O."""
+    B, H = 2, 2
+    q, k, v = synth.outlier_inputs(B, H, N, D, "bf16", seed=5)
+    signs = synth.hadamard_signs(H, D, seed=5)
+    qr, kr = oracle.hadamard_rotate(q, signs), oracle.hadamard_rotate(k, signs)
+    (qc, qs), (kc, ks), (vc, vs) = (oracle.block_quantize(t) for t in (qr, kr, v))
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    o, lse = attn.attn_fwd_fp8(dev(qc), dev(kc), dev(vc), dev(qs), dev(ks), dev(vs), causal=causal)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.attention(oracle.dequantize(qc, qs), oracle.dequantize(kc, ks),
+                                      oracle.dequantize(vc, vs), causal=causal, scale=D ** -0.5)
+    d = o.double().cpu().numpy() - o_ref
+    assert np.isfinite(d).all()
+    assert np.abs(lse.double().cpu().numpy() - lse_ref).max() <= 1e-3
+    assert np.sqrt(np.mean(d ** 2)) <= 0.08 * np.sqrt(np.mean(o_ref ** 2))
+    assert attn.device_status() == attn.ATTN_OK
+
+
+def test_fp8_weights_layout_through_identity_values():
+    """V = identity (N = d = 128, one key block): O equals the rounded softmax
+    weights themselves, so every weight is checked at its position: within an
+    E4M3 half step (2^-4 relative, 2^-10 absolute below 2^-6) of the exact one."""
+    N = 128
+    q, k, _ = synth.attention_inputs(1, 2, N, D, "bf16", seed=6)
+    v = torch.eye(N, D, dtype=torch.bfloat16).expand(1, 2, N, D).contiguous()
+    for causal in (False, True):
+        o, lse = attn.attn_fwd_fp8_pipeline(q.cuda(), k.cuda(), v.cuda(), signs=None, causal=causal)
+        torch.cuda.synchronize()
+        q8, k8, v8, qs, ks, vs = attn.fp8_prepare(q.cuda(), k.cuda(), v.cuda())
+        deq = [oracle.dequantize(_np(c), _np(s)) for c, s in ((q8, qs), (k8, ks), (v8, vs))]
+        w_ref, lse_ref = oracle.attention(deq[0], deq[1], deq[2], causal=causal, scale=D ** -0.5)
+        w = o.double().cpu().numpy()
+        # The kernel's running sum is >= 1 (the row maximum contributes 2^0), so
+        # a weight below the E4M3 normal range (2^-6) is off by at most 2^-10.
+        tol = 2.0 ** -4 * w_ref + 2.0 ** -10 + 2.0 ** -8 * w_ref + 1e-6
+        assert np.all(np.abs(w - w_ref) <= tol), (causal, np.abs(w - w_ref).max())
+
+
+@pytest.mark.parametrize("N", [1024, 2048, 4096, 8192, 16384])
+def test_fp8_error_against_exact_attention(N):
+    """FP8 path with per-block scales and the Hadamard rotation on inputs with
+    0.1 % outliers (B = 16384 / N, H = 16, d = 128): RMS <= 2.5e-2 against
+    exact attention on the 16-bit inputs (sampled rows); the naive per-tensor
+    FP8 baseline is computed on the same rows and reported."""
+    B, H = 16384 // N, 16
+    q, k, v = synth.outlier_inputs(B, H, N, D, "bf16", seed=0)
+    signs = synth.hadamard_signs(H, D, seed=0)
+    rows = synth.sample_rows(N, 32, seed=0, salt=N)
+    heads = [0, B * H // 2, B * H - 1]
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    o8, _ = attn.attn_fwd_fp8_pipeline(qc, kc, vc, signs=signs.cuda())
+    ob, _ = attn.attn_fwd_fp8_pipeline(qc, kc, vc, signs=None, per_tensor=True)
+    torch.cuda.synchronize()
+    flat = lambda t: t.reshape(1, B * H, N, D)
+    err8, errb = [], []
+    for h in heads:
+        sl = slice(h, h + 1)
+        o_ref, _ = oracle.attention(flat(q)[:, sl], flat(k)[:, sl], flat(v)[:, sl], scale=D ** -0.5,
+                                    rows=rows)
+        idx = torch.as_tensor(rows, device="cuda")
+        err8.append(flat(o8)[:, sl][:, :, idx].double().cpu().numpy() - o_ref)
+        errb.append(flat(ob)[:, sl][:, :, idx].double().cpu().numpy() - o_ref)
+    rms8 = float(np.sqrt(np.mean(np.concatenate(err8) ** 2)))
+    rmsb = float(np.sqrt(np.mean(np.concatenate(errb) ** 2)))
+    print(f"N={N}: FP8 per-block + Hadamard RMS {rms8:.3e}; naive per-tensor FP8 RMS {rmsb:.3e}; "
+          f"ratio {rmsb / rms8:.2f}")
+    assert rms8 <= FP8_RMS
+    assert attn.device_status() == attn.ATTN_OK
+
+
+def test_fp8_empty_and_bad_arguments():
+    z = torch.empty((1, 1, 0, D), dtype=torch.bfloat16, device="cuda")
+    attn.fp8_prepare(z, z, z)
+    q = torch.zeros((1, 1, 16, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(attn.AttnError) as e:
+        attn.fp8_prepare(q, q, q)
+    assert e.value.status == attn.ATTN_ERR_UNSUPPORTED
