@@ -264,3 +264,38 @@ def debug_bounded_wait(timeout_ns: int, stream=None) -> None:
     dev = torch.cuda.current_device()
     _check(_load().attn_debug_bounded_wait(int(timeout_ns), _stream_handle(stream, dev)),
            "attn_debug_bounded_wait")
+
+
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024  # ATTN_NOALLOC_SCRATCH_BYTES in include/attn.h
+
+
+def attn_fwd_host_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                          scale: float | None = None, out: torch.Tensor | None = None,
+                          lse: torch.Tensor | None = None, device=None, stream=None):
+    """attn_fwd_host without a workspace, for callers that cannot allocate
+    device memory (a host framework that owns every device allocation, device
+    memory fully reserved by another allocator, or a latency-critical path where
+    cudaMalloc could synchronise the device).  The library keeps the device
+    copies in one fixed array of NOALLOC_SCRATCH_BYTES shared by every call:
+    larger problems raise ATTN_ERR_INVALID_ARG, and calls whose GPU work
+    overlaps race on the array.  Host output tensors are created here when not
+    given (host memory only)."""
+    B, H, N, d = _shape_of(q, k, v)
+    if q.is_cuda:
+        raise ValueError("attn_fwd_host_noalloc takes host tensors")
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q, pin_memory=q.is_pinned())
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=q.is_pinned())
+    fn = _load().attn_fwd_host_noalloc
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    fn.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32, vp]
+    fn.restype = i32
+    with torch.cuda.device(device):
+        st = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, d,
+                int(bool(causal)), float(scale), _DTYPES[q.dtype], _stream_handle(stream, device))
+    _check(st, "attn_fwd_host_noalloc")
+    return out, lse

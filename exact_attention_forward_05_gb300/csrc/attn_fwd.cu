@@ -2,6 +2,7 @@
 // argument checks and dispatch to attn_kernel::attn_fwd_kernel<D, kind>
 // (attn_kernel.cuh), the host-buffer entry point, and the bounded-wait probe.
 #include <cmath>
+#include <mutex>
 
 #include "attn_kernel.cuh"
 
@@ -121,4 +122,55 @@ ATTN_EXPORT attn_status attn_fwd_host(const void* q_host, const void* k_host, co
 ATTN_EXPORT attn_status attn_debug_bounded_wait(uint64_t timeout_ns, void* stream) {
   debug_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(timeout_ns);
   return attn_internal::cuda_status(cudaGetLastError());
+}
+
+// ---------------------------------------------------------------------------
+// Host-buffer entry point that allocates nothing.
+//
+// Some callers cannot allocate device memory: plugins whose host framework owns
+// every device allocation through its own pool and forbids allocating inside a
+// plugin call; processes whose device memory is already reserved in full by
+// another allocator, where a cudaMalloc would fail; and latency-critical code,
+// where cudaMalloc / cudaFree may synchronise the device and stall other work.
+// For them the device copies that attn_fwd_host keeps in a caller-provided
+// workspace live instead in one fixed array in this module's device memory.
+// Every GPU that loads the library holds the array until the process exits.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(ATTN_NOALLOC_SCRATCH_BYTES);
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the array, looked up once per device (with that device
+// current).  In host code the symbol itself is only a host-side stand-in.
+attn_status noalloc_scratch_address(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return attn_internal::cuda_status(e);
+  if (dev < 0 || dev >= 64) return ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return attn_internal::cuda_status(e);
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return ATTN_OK;
+}
+
+}  // namespace
+
+ATTN_EXPORT attn_status attn_fwd_host_noalloc(const void* q_host, const void* k_host,
+                                              const void* v_host, void* o_host, float* lse_host,
+                                              int B, int H, int N, int d, int causal, float scale,
+                                              attn_dtype dtype, void* stream) {
+  attn_status st = check_args(q_host, k_host, v_host, o_host, lse_host, B, H, N, d, scale, dtype);
+  if (st != ATTN_OK || static_cast<int64_t>(B) * H * N == 0) return st;
+  if (attn_fwd_host_workspace_bytes(B, H, N, d, dtype) > kNoAllocScratchBytes) return ATTN_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch_address(&scratch)) != ATTN_OK) return st;
+  return attn_fwd_host(q_host, k_host, v_host, o_host, lse_host, B, H, N, d, causal, scale, dtype,
+                       scratch, kNoAllocScratchBytes, stream);
 }

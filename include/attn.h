@@ -97,6 +97,37 @@ attn_status attn_fwd_host(const void* q_host, const void* k_host, const void* v_
                           attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_fwd_host_noalloc -- attn_fwd_host for callers that cannot allocate device
+ * memory, with no workspace argument.  The paper has no counterpart: this is a
+ * deployment variant of the host-buffer entry point.
+ *
+ * Who needs it: plugins whose host framework owns all device memory and forbids
+ * allocating inside a call, processes whose device memory is fully reserved by
+ * another allocator (a cudaMalloc would fail), and latency-critical callers
+ * (cudaMalloc / cudaFree may synchronise the device).
+ *
+ * The device copies of Q, K, V, O and lse live in one fixed array of
+ * ATTN_NOALLOC_SCRATCH_BYTES inside the library's device memory, held by every
+ * GPU that loads the library until the process exits.  The call allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library routine).
+ *  - Size limit: returns ATTN_ERR_INVALID_ARG, launching nothing, when
+ *    attn_fwd_host_workspace_bytes(B, H, N, d, dtype) exceeds
+ *    ATTN_NOALLOC_SCRATCH_BYTES.
+ *  - Set-up: the first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - Sharing: every call uses the same array, which keeps the last call's
+ *    contents; nothing in it has to start at zero (each call writes every byte
+ *    it reads).  Calls whose GPU work overlaps (other host threads or streams
+ *    at the same time) race on the array and must not be issued.
+ * Other arguments, copies and synchronisation as for attn_fwd_host.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+attn_status attn_fwd_host_noalloc(const void* q_host, const void* k_host, const void* v_host,
+                                  void* o_host, float* lse_host, int B, int H, int N, int d,
+                                  int causal, float scale, attn_dtype dtype, void* stream);
+
+/*
  * attn_fp8_prepare -- FP8 pre-pass: incoherent processing and block quantisation
  * ("Incoherent Processing for FP8 Accuracy", FlashAttention-3 podcast page;
  * comrad404 review, "Метод", item 3).
