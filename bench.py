@@ -291,6 +291,8 @@ def run_gpu(args):
     e2e_s = max_over_ranks(time.perf_counter() - t0, world) / e2e_steps
     e2e_value = flops(w) * world / e2e_s / 1e12
 
+    fp8 = fp8_leg(w, dev, stream, rank, args) if w["d"] == 128 else None
+
     peak, peak_src = peaks()
     achieved = flops(w) / (ms / args.steps * 1e-3) / 1e12
     line = None
@@ -321,6 +323,7 @@ def run_gpu(args):
             "gpu_launches": n_launch,
             "clocks": clocks,
             "other_mask": {"causal": other["causal"], "value": round(other_value, 2), "unit": UNIT},
+            "fp8": fp8,
             "parity_sample": par,
             "device": torch.cuda.get_device_name(dev),
         }
@@ -328,6 +331,69 @@ def run_gpu(args):
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
     return line
+
+
+def fp8_leg(w, dev, stream, rank, args):
+    """The FP8 path on the same shapes with 0.1 % outliers in Q, K, V: the FP8
+    attention kernel alone (against the FP8 dense peak = 2 x the measured bf16
+    peak, the nominal FP8/BF16 ratio of the tensor cores), the pre-pass
+    (Hadamard rotation + block quantisation, HBM-bound) and the two together;
+    plus the RMS error against exact attention on sampled rows next to the
+    naive per-tensor FP8 baseline."""
+    import exact_attention_forward_05_gb300 as attn
+    import synth
+    B, H, N, d = w["B"], w["H"], w["N"], w["d"]
+    q, k, v = synth.outlier_inputs(B, H, N, d, "bf16", seed=rank)
+    signs = synth.hadamard_signs(H, d, seed=rank).to(dev)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    nblk = (N + 127) // 128
+    bufs = [torch.empty((B, H, N, d), dtype=torch.uint8, device=dev) for _ in range(3)] + \
+           [torch.empty((B, H, nblk), dtype=torch.float32, device=dev) for _ in range(3)]
+    o8 = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    l8 = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    scale = d ** -0.5
+    prep = lambda: attn.fp8_prepare(qd, kd, vd, signs=signs, out=bufs, stream=stream)
+    fwd = lambda: attn.attn_fwd_fp8(*bufs, causal=w["causal"], scale=scale, out=o8, lse=l8, stream=stream)
+    def both():
+        prep()
+        fwd()
+    n = max(args.steps // 4, 5)
+    prep()
+    t_fwd = time_kernel(fwd, n, 3, stream) / n
+    t_prep = time_kernel(prep, n, 3, stream) / n
+    t_both = time_kernel(both, n, 3, stream) / n
+    if attn.device_status() != attn.ATTN_OK:
+        raise RuntimeError("device status after the FP8 leg")
+    peak = 2.0 * peaks()[0]
+    fl = flops(w)
+    out = {"workload": f"fp8 e4m3 attention fwd, B={B}, H={H}, N={N}, d={d}, "
+                       f"{'causal' if w['causal'] else 'non-causal'}, per-block scales + Hadamard, "
+                       "inputs N(0,1) + N(0,100) * Bernoulli(0.001), bf16 output",
+           "value": round(fl / (t_fwd * 1e-3) / 1e12, 2), "unit": UNIT,
+           "roofline": {"bound": "tensor", "achieved": round(fl / (t_fwd * 1e-3) / 1e12, 2),
+                        "peak": peak, "frac": round(fl / (t_fwd * 1e-3) / 1e12 / peak, 4),
+                        "peak_source": "2 x measured bf16 burst (nominal FP8 / BF16 dense ratio)",
+                        "kernel": "attn_fwd_kernel<128, e4m3>"},
+           "prepare_us": round(t_prep * 1e3, 2),
+           "prepare_gbs": round((3 * q.numel() * 2 + 3 * q.numel() + 3 * B * H * nblk * 4) / (t_prep * 1e-3) / 1e9, 1),
+           "pipeline_value": round(fl / (t_both * 1e-3) / 1e12, 2)}
+    if rank == 0:
+        import oracle
+        rows = synth.sample_rows(N, 16, seed=0, salt=11)
+        idx = torch.as_tensor(rows, device=dev)
+        ob, _ = attn.attn_fwd_fp8_pipeline(qd, kd, vd, signs=None, causal=w["causal"], scale=scale,
+                                           per_tensor=True)
+        e8, eb = [], []
+        for h in (0, B * H - 1):
+            bsel, hsel = divmod(h, H)
+            sl = (slice(bsel, bsel + 1), slice(hsel, hsel + 1))
+            o_ref, _ = oracle.attention(q[sl], k[sl], v[sl], causal=w["causal"], scale=scale, rows=rows)
+            e8.append(o8[sl][:, :, idx].double().cpu().numpy() - o_ref)
+            eb.append(ob[sl][:, :, idx].double().cpu().numpy() - o_ref)
+        out["rms"] = float(np.sqrt(np.mean(np.concatenate(e8) ** 2)))
+        out["rms_naive_per_tensor"] = float(np.sqrt(np.mean(np.concatenate(eb) ** 2)))
+        out["rms_rows"] = f"{len(rows)} rows x 2 heads"
+    return out
 
 
 # --------------------------------------------------------- reference arm

@@ -190,19 +190,28 @@ FP8_BLOCK = 128  # rows per quantisation scale block
 
 
 def fp8_prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, signs: torch.Tensor | None = None,
-                per_tensor: bool = False, stream=None):
+                per_tensor: bool = False, stream=None, out=None):
     """FP8 pre-pass on CUDA tensors [B, H, N, 128] (fp16 or bf16): random-sign
     Hadamard rotation of Q and K (when ``signs`` [H, 128] int8 is given) and
     E4M3 quantisation with one float32 scale per 128 rows of a head (or one per
     tensor).  Returns (q8, k8, v8, q_scale, k_scale, v_scale); the codes are
-    uint8 tensors [B, H, N, 128]."""
+    uint8 tensors [B, H, N, 128].  ``out`` may pass those six tensors in."""
     B, H, N, d = _shape_of(q, k, v)
     if not q.is_cuda:
         raise ValueError("fp8_prepare takes CUDA tensors")
     nblk = (N + FP8_BLOCK - 1) // FP8_BLOCK
-    codes = [torch.empty((B, H, N, d), dtype=torch.uint8, device=q.device) for _ in range(3)]
     sshape = (1,) if per_tensor else (B, H, nblk)
-    scales = [torch.empty(sshape, dtype=torch.float32, device=q.device) for _ in range(3)]
+    if out is not None:
+        codes, scales = list(out[:3]), list(out[3:])
+        for c in codes:
+            if c.dtype != torch.uint8 or tuple(c.shape) != (B, H, N, d) or not c.is_contiguous():
+                raise ValueError("code tensors must be contiguous uint8 [B, H, N, d]")
+        for sc in scales:
+            if sc.dtype != torch.float32 or tuple(sc.shape) != sshape or not sc.is_contiguous():
+                raise ValueError(f"scale tensors must be contiguous float32 {sshape}")
+    else:
+        codes = [torch.empty((B, H, N, d), dtype=torch.uint8, device=q.device) for _ in range(3)]
+        scales = [torch.empty(sshape, dtype=torch.float32, device=q.device) for _ in range(3)]
     if signs is not None:
         if signs.dtype != torch.int8 or tuple(signs.shape) != (H, d):
             raise ValueError("signs must be an int8 [H, d] tensor of +1 / -1")

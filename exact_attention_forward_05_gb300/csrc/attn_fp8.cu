@@ -20,7 +20,7 @@ namespace {
 
 constexpr int kHeadDim = 128;     // FP8 path: d = 128
 constexpr int kQuantRows = 128;   // rows per scale block
-constexpr int kPrepThreads = 256; // 8 warps x 16 rows each
+constexpr int kPrepThreads = 512; // 16 warps x 8 rows each: 32 values per thread
 constexpr float kE4M3Max = 448.0f;
 
 enum PrepMode : int { PREP_BLOCK = 0, PREP_AMAX = 1, PREP_QUANT_GLOBAL = 2 };
@@ -61,12 +61,18 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const PrepPar
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool rotate = t < 2 && p.signs != nullptr;
   const size_t head = static_cast<size_t>(bh) * p.N * kHeadDim;
-  const uint8_t* src = static_cast<const uint8_t*>(p.src[t]);
+  // Operands chosen by selects, not by indexing the parameter arrays (which
+  // would copy them to local memory).
+  const uint8_t* src = static_cast<const uint8_t*>(t == 0 ? p.src[0] : t == 1 ? p.src[1] : p.src[2]);
+  float* scale_t = t == 0 ? p.scale[0] : t == 1 ? p.scale[1] : p.scale[2];
+  uint8_t* dst = t == 0 ? p.dst[0] : t == 1 ? p.dst[1] : p.dst[2];
 
-  float x[16][4];
+  constexpr int kWarps = kPrepThreads / 32;
+  constexpr int kRowsPerWarp = kQuantRows / kWarps;
+  float x[kRowsPerWarp][4];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int row = blk * kQuantRows + warp + 8 * i;
+  for (int i = 0; i < kRowsPerWarp; ++i) {
+    const int row = blk * kQuantRows + warp + kWarps * i;
     if (row < p.N) {
       const uint2 raw = *reinterpret_cast<const uint2*>(src + (head + static_cast<size_t>(row) * kHeadDim + 4 * lane) * 2);
       if constexpr (BF16IN) {
@@ -87,7 +93,7 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const PrepPar
     const float s0 = sg[0], s1 = sg[1], s2 = sg[2], s3 = sg[3];
     const float inv_sqrt_d = 0.08838834764831845f;  // 1 / sqrt(128)
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < kRowsPerWarp; ++i) {
       x[i][0] *= s0; x[i][1] *= s1; x[i][2] *= s2; x[i][3] *= s3;
       fwht128(x[i], lane);
 #pragma unroll
@@ -99,7 +105,7 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const PrepPar
   __shared__ float warp_max[kPrepThreads / 32];
   float a = 0.f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i)
+  for (int i = 0; i < kRowsPerWarp; ++i)
 #pragma unroll
     for (int e = 0; e < 4; ++e) a = fmaxf(a, fabsf(x[i][e]));
 #pragma unroll
@@ -111,21 +117,20 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const PrepPar
   for (int w = 0; w < kPrepThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
 
   if constexpr (MODE == PREP_AMAX) {
-    if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned int*>(p.scale[t]), __float_as_uint(amax));
+    if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned int*>(scale_t), __float_as_uint(amax));
     return;
   } else {
     float s;
     if constexpr (MODE == PREP_BLOCK) {
       s = amax > 0.f ? amax / kE4M3Max : 1.f;
-      if (threadIdx.x == 0) p.scale[t][static_cast<size_t>(bh) * p.nblk + blk] = s;
+      if (threadIdx.x == 0) scale_t[static_cast<size_t>(bh) * p.nblk + blk] = s;
     } else {
-      const float g = __uint_as_float(*reinterpret_cast<const unsigned int*>(p.scale[t]));
+      const float g = __uint_as_float(*reinterpret_cast<const unsigned int*>(scale_t));
       s = g > 0.f ? g / kE4M3Max : 1.f;
     }
-    uint8_t* dst = p.dst[t];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int row = blk * kQuantRows + warp + 8 * i;
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+      const int row = blk * kQuantRows + warp + kWarps * i;
       if (row >= p.N) continue;
       const uint32_t lo = __nv_cvt_float2_to_fp8x2(
           make_float2(__fdiv_rn(x[i][0], s), __fdiv_rn(x[i][1], s)), __NV_SATFINITE, __NV_E4M3);

@@ -482,12 +482,17 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         } else {
           float mx;
           if (cj >= 0.f) {
-            mx = -INFINITY;
+            float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
-              for (int i = 0; i < 32; i += 2)
-                mx = max3(mx, __uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1]));
+              for (int i = 0; i < 32; i += 8) {
+                m0 = max3(m0, __uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1]));
+                m1 = max3(m1, __uint_as_float(s[c][i + 2]), __uint_as_float(s[c][i + 3]));
+                m2 = max3(m2, __uint_as_float(s[c][i + 4]), __uint_as_float(s[c][i + 5]));
+                m3 = max3(m3, __uint_as_float(s[c][i + 6]), __uint_as_float(s[c][i + 7]));
+              }
+            mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
           } else {
             mx = INFINITY;
 #pragma unroll
@@ -513,25 +518,22 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         float rowsum = 0.f;
         const float neg_m = lg2_ratio - m_used;
         if constexpr (!F8) {
+          float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+          const float2 c2 = masked ? make_float2(1.f, 1.f) : make_float2(cj, cj);
+          const float2 m2 = make_float2(neg_m, neg_m);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float x0 = __uint_as_float(s[c][2 * i]), x1 = __uint_as_float(s[c][2 * i + 1]);
-              float p0, p1;
-              if (masked) {
-                p0 = ex2(x0 + neg_m);
-                p1 = ex2(x1 + neg_m);
-              } else {
-                p0 = ex2(fmaf(x0, cj, neg_m));
-                p1 = ex2(fmaf(x1, cj, neg_m));
-              }
-              rowsum += p0 + p1;
-              pk[i] = pack2<KIND>(p0, p1);
+              const float2 a = ffma2(make_float2(__uint_as_float(s[c][2 * i]), __uint_as_float(s[c][2 * i + 1])), c2, m2);
+              const float2 pp = make_float2(ex2(a.x), ex2(a.y));
+              if (i & 1) acc1 = fadd2(acc1, pp); else acc0 = fadd2(acc0, pp);
+              pk[i] = pack2<KIND>(pp.x, pp.y);
             }
             tmem_st16(tm_s + 16 * c, pk);
           }
+          rowsum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
         } else {
           uint32_t pk[32];
 #pragma unroll
