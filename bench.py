@@ -35,7 +35,8 @@ import torch  # noqa: E402
 METRIC = "attention fwd TFLOP/s and % of GB300 dense BF16/FP8 tensor peak vs seq len"
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
-KERNEL_SOURCE = os.path.join(ROOT, "exact_attention_forward_05_gb300", "csrc", "attn_fwd.cu")
+KERNEL_SOURCES = [os.path.join(ROOT, "exact_attention_forward_05_gb300", "csrc", f)
+                  for f in ("attn_kernel.cuh", "sm103.cuh", "attn_fwd.cu")]
 PROFILE_JSON = os.path.join(ROOT, "profiles", "attn_fwd_bf16_b2_h16_n8192_d128.json")
 
 WORKLOADS = {}
@@ -151,17 +152,31 @@ def time_kernel(fn, steps: int, warmup: int, stream):
 
 
 def barrier(world):
+    """All ranks meet (process group barrier), then this rank's GPU work drains."""
     if world > 1:
         torch.distributed.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The largest value of x over all ranks (the elapsed time of the slowest
+    rank); the reduction runs on the process group's own device (CUDA for
+    NCCL, host memory for gloo)."""
     if world == 1:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    on_gpu = torch.distributed.get_backend() == "nccl"
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if on_gpu else "cpu")
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def kernel_source_sha256() -> str:
+    """Hash of the sources the bf16 attention kernel is built from."""
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()
 
 
 def traffic_from_profile():
@@ -171,7 +186,7 @@ def traffic_from_profile():
         return None
     with open(PROFILE_JSON) as f:
         prof = json.load(f)
-    sha = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()
+    sha = kernel_source_sha256()
     if prof.get("kernel_source_sha256") != sha:
         return None
     return prof.get("dram_bytes_per_launch_full_workload")
@@ -440,6 +455,47 @@ def run_reference(args):
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_sweep(args):
+    """One device-timed line per point of the sequence-length sweep (bf16,
+    B = 16384/N, H = 2048/d, causal and non-causal), and the FP8 kernel at
+    d = 128 (H = 16, inputs with 0.1 % outliers).  Same timing as the main
+    line: CUDA events on the launching stream around ``--steps`` launches."""
+    import exact_attention_forward_05_gb300 as attn
+    import synth
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    peak = peaks()[0]
+
+    def emit(w, ms, pk):
+        tf = flops(w) / (ms * 1e-3) / 1e12
+        print(json.dumps({"workload": describe(w), "value": round(tf, 1), "unit": UNIT,
+                          "frac": round(tf / pk, 4), "ms": round(ms, 4)}), flush=True)
+
+    for N in (512, 1024, 2048, 4096, 8192, 16384):
+        for d in (64, 128, 256):
+            B, H = 16384 // N, 2048 // d
+            q, k, v = (t.to(dev) for t in synth.attention_inputs(B, H, N, d, "bf16", seed=0))
+            o = torch.empty_like(q)
+            lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+            for causal in (False, True):
+                f = lambda: attn.attn_fwd(q, k, v, causal=causal, scale=d ** -0.5, out=o, lse=lse,
+                                          stream=stream)
+                emit(dict(B=B, H=H, N=N, d=d, causal=causal, dtype="bf16"),
+                     time_kernel(f, args.steps, args.warmup, stream) / args.steps, peak)
+            del q, k, v, o, lse
+        B, H, d = 16384 // N, 16, 128
+        q, k, v = (t.to(dev) for t in synth.outlier_inputs(B, H, N, d, "bf16", seed=0))
+        bufs = attn.fp8_prepare(q, k, v, signs=synth.hadamard_signs(H, d, seed=0).to(dev))
+        o8 = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+        for causal in (False, True):
+            f = lambda: attn.attn_fwd_fp8(*bufs, causal=causal, scale=d ** -0.5, out=o8,
+                                          return_lse=False, stream=stream)
+            emit(dict(B=B, H=H, N=N, d=d, causal=causal, dtype="fp8 e4m3"),
+                 time_kernel(f, args.steps, args.warmup, stream) / args.steps, 2 * peak)
+    if attn.device_status() != attn.ATTN_OK:
+        raise RuntimeError("device status after the sweep")
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -447,7 +503,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--sweep", action="store_true",
+                    help="print one device-timed line per sweep configuration instead")
     args = ap.parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     line = run_reference(args) if args.impl == "reference" else run_gpu(args)
