@@ -112,7 +112,8 @@ struct FwdParams {
   int causal;
   float sl2;  // scale * log2(e)
   int units_per_head;
-  int num_units;
+  int num_units;   // work entries: [0, full_units) whole units, then half units
+  int full_units;
   uint64_t timeout_ns;
   // FP8 only: scales, element (bh, block) at [bh * bh_stride + block * blk_stride].
   const float* q_scale;
@@ -128,10 +129,17 @@ struct Unit {
 
 // Unit order: causal units longest-first (highest query block first, all heads
 // of one query block together); full attention head-major so that CTAs that
-// run at the same time share K/V through L2.
+// run at the same time share K/V through L2.  Entries from full_units on are
+// half units: the two Q tiles of one of the last units, one entry each, so that
+// a short last round of the persistent schedule costs half a unit.
 template <int NQ>
-__device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
+__device__ __forceinline__ Unit decode_unit(int e, const FwdParams& p) {
   Unit w;
+  int u = e, half = -1;
+  if (e >= p.full_units) {
+    u = p.full_units + (e - p.full_units) / 2;
+    half = (e - p.full_units) & 1;
+  }
   int qu;
   if (p.causal) {
     qu = p.units_per_head - 1 - u / p.BH;
@@ -140,12 +148,12 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
     w.bh = u / p.units_per_head;
     qu = u % p.units_per_head;
   }
-  w.m0 = qu * kBM * NQ;
+  w.m0 = qu * kBM * NQ + (half > 0 ? kBM : 0);
   w.nkb = (p.N + kBN - 1) / kBN;
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int r0 = w.m0 + kBM * t;
-    if (t >= NQ || r0 >= p.N)
+    if (t >= NQ || r0 >= p.N || (half >= 0 && t > 0))
       w.nb[t] = 0;
     else
       w.nb[t] = p.causal ? min(w.nkb, r0 / kBN + 1) : w.nkb;
@@ -263,6 +271,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         if (u < 0) continue;
         const Unit w = decode_unit<NQ>(u, p);
         const int nbmax = max(w.nb[0], w.nb[1]);
+        if (nbmax == 0) continue;  // no query row of this entry is below N
         if (!mbar_wait(BAR(C::B_Q_EMPTY), (q_iter & 1u) ^ 1u, wc, attn_internal::kStatusTimeoutLoad)) {
           ok = false;
           break;
@@ -346,6 +355,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         if (u < 0) continue;
         const Unit w = decode_unit<NQ>(u, p);
         const int nbmax = max(w.nb[0], w.nb[1]);
+        if (nbmax == 0) continue;
         if (!mbar_wait(BAR(C::B_Q_FULL), q_iter & 1u, wc, attn_internal::kStatusTimeoutMma)) { ok = false; break; }
         ++q_iter;
         tc_fence_after();
@@ -535,21 +545,27 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
           }
           rowsum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
         } else {
-          uint32_t pk[32];
+          // E4M3 weights, four per TMEM column; each 32-column chunk is stored
+          // as soon as it is packed.
+          float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+          const float2 c2 = masked ? make_float2(1.f, 1.f) : make_float2(cj, cj);
+          const float2 m2 = make_float2(neg_m, neg_m);
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c) {
+            uint32_t pk[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              float pv[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float x = __uint_as_float(s[c][4 * i + e]);
-                pv[e] = masked ? ex2(x + neg_m) : ex2(fmaf(x, cj, neg_m));
-              }
-              rowsum += (pv[0] + pv[1]) + (pv[2] + pv[3]);
-              pk[8 * c + i] = pack4_e4m3(pv[0], pv[1], pv[2], pv[3]);
+              const float2 a = ffma2(make_float2(__uint_as_float(s[c][4 * i]), __uint_as_float(s[c][4 * i + 1])), c2, m2);
+              const float2 bq = ffma2(make_float2(__uint_as_float(s[c][4 * i + 2]), __uint_as_float(s[c][4 * i + 3])), c2, m2);
+              const float2 p01 = make_float2(ex2(a.x), ex2(a.y));
+              const float2 p23 = make_float2(ex2(bq.x), ex2(bq.y));
+              acc0 = fadd2(acc0, p01);
+              acc1 = fadd2(acc1, p23);
+              pk[i] = pack4_e4m3(p01.x, p01.y, p23.x, p23.y);
             }
-          tmem_st32(tm_s, pk);
+            tmem_st8(tm_s + 8 * c, pk);
+          }
+          rowsum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
         }
 
         if (j > 0) {
@@ -646,10 +662,25 @@ attn_status launch_fwd(const void* q, const void* k, const void* v, FwdParams pr
   prm.N = N;
   prm.sl2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.units_per_head = (N + kBM * C::NQ - 1) / (kBM * C::NQ);
-  prm.num_units = prm.units_per_head * prm.BH;
+  const int units = prm.units_per_head * prm.BH;
   prm.timeout_ns = attn_internal::wait_timeout_ns();
   const int sms = attn_internal::sm_count();
   if (sms <= 0) return ATTN_ERR_CUDA;
+  // Full attention with two Q tiles per unit: when the last round of the
+  // persistent schedule would be at most half full, its units are split into
+  // half units (one Q tile each, one per CTA), so that round costs half a unit.
+  prm.full_units = units;
+  prm.num_units = units;
+  if (C::NQ == 2 && !prm.causal) {
+    const int rest = units % sms;
+    if (units <= sms / 2) {
+      prm.full_units = 0;
+      prm.num_units = 2 * units;
+    } else if (units > sms && rest > 0 && 2 * rest <= sms) {
+      prm.full_units = units - rest;
+      prm.num_units = units + rest;
+    }
+  }
   const int grid = prm.num_units < sms ? prm.num_units : sms;
   attn_fwd_kernel<D, KIND><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, prm);
   return attn_internal::cuda_status(cudaGetLastError());
