@@ -87,7 +87,15 @@ struct Cfg {
   static constexpr int SOFTMAX_WARPS = 4 * NQ;
   static constexpr int LOAD_WARP = SOFTMAX_WARPS;
   static constexpr int MMA_WARP = SOFTMAX_WARPS + 1;
-  static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 2);
+  // Two Q tiles: three whole warpgroups (softmax, softmax, load + MMA + two
+  // idle warps), so that the softmax warpgroups can take registers from the
+  // third one with setmaxnreg: 2 x 128 x 208 + 128 x 88 = 384 x 168, the
+  // registers the CTA is launched with.  One Q tile: six warps, no split.
+  static constexpr bool REG_SPLIT = NQ == 2;
+  static constexpr int SOFTMAX_REGS = 208, OTHER_REGS = 88;
+  static constexpr int THREADS = REG_SPLIT ? 384 : 32 * (SOFTMAX_WARPS + 2);
+  static_assert(!REG_SPLIT || 2 * 128 * SOFTMAX_REGS + 128 * OTHER_REGS <= THREADS * 168,
+                "register split exceeds the launch allocation");
   // TMEM columns: two S buffers, then the O accumulator(s).
   static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + D;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -246,6 +254,10 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // The register budget changes inside each warpgroup's own branch, so that
+  // the compiler allocates every role's code against its own budget.
+  if (warp >= C::SOFTMAX_WARPS) {
+  if constexpr (C::REG_SPLIT) setmaxnreg_dec<C::OTHER_REGS>();
   if (warp == C::LOAD_WARP) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -415,8 +427,10 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
       mma_commit(BAR(C::B_MMA_DONE));
       mbar_drain(BAR(C::B_MMA_DONE), 0, 100000000ull);
     }
+  }
   } else {
     // ------------------------------------------------------------ softmax
+    if constexpr (C::REG_SPLIT) setmaxnreg_inc<C::SOFTMAX_REGS>();
     const WaitCtx wc{abort_flag, &g_status_word, p.timeout_ns};
     const int wg = warp >> 2;                 // Q tile / O accumulator of this group
     const int wq = warp & 3;                  // TMEM lane quarter of this warp

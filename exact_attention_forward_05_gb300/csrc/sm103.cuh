@@ -109,6 +109,19 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, co
   }
 }
 
+// ------------------------------------------------------- register budgets
+
+// Warpgroup-wide change of the per-thread register allocation (all four warps
+// of a warpgroup execute it with the same count).
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // -------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch(const CUtensorMap* map) {
