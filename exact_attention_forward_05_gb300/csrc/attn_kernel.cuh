@@ -84,6 +84,11 @@ struct Cfg {
   static constexpr int PV_STEPS = kBN / KSTEP;
   static constexpr int P_COLS = kBN * ELEM / 4;  // TMEM columns holding one row of P
   static constexpr int STAGES = KIND == KIND_E4M3 ? 8 : (D == 64 ? 6 : (D == 128 ? 4 : 2));
+  // Two Q tiles: the stages form pairs, one per key-block step j holding K_j
+  // and V_{j-1} (consumed and released together), with one full and one
+  // empty barrier per pair.  One Q tile: single-tile stages.
+  static constexpr bool KV_PAIRS = NQ == 2;
+  static constexpr int RING = KV_PAIRS ? STAGES / 2 : STAGES;
   static constexpr int SOFTMAX_WARPS = 4 * NQ;
   // Two Q tiles, E4M3: the products P_{j-1} V_{j-1} signal nothing of their
   // own; the softmax learns of their completion from the S_FULL commit of the
@@ -282,6 +287,27 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         ++kv_fill;
         return true;
       };
+      // Pair slot s holds K_j in tile 2s and V_{j-1} in tile 2s+1 (either may
+      // be absent at the ends of a unit: step 0 has no V, step nbmax no K).
+      auto load_pair = [&](int j, int nbmax, int bh) -> bool {
+        const uint32_t s = kv_fill % C::RING;
+        const uint32_t ph = (kv_fill / C::RING) & 1u;
+        if (!mbar_wait(BAR(C::B_KV_EMPTY + s), ph ^ 1u, wc, attn_internal::kStatusTimeoutLoad))
+          return false;
+        const bool has_k = j < nbmax, has_v = j >= 1;
+        mbar_arrive_expect_tx(BAR(C::B_KV_FULL + s), (has_k + has_v) * C::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::CHUNKS; ++c) {
+          if (has_k)
+            tma_load_3d(sKV + (2 * s) * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmK,
+                        BAR(C::B_KV_FULL + s), c * C::CHUNK_ELEMS, j * kBN, bh);
+          if (has_v)
+            tma_load_3d(sKV + (2 * s + 1) * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmV,
+                        BAR(C::B_KV_FULL + s), c * C::CHUNK_ELEMS, (j - 1) * kBN, bh);
+        }
+        ++kv_fill;
+        return true;
+      };
       for (int r = 0; ok; ++r) {
         if (r * static_cast<int>(gridDim.x) >= p.num_units) break;
         const int u = unit_of_round(r, p.num_units);
@@ -305,15 +331,19 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         }
         // K/V in the order the MMA warp consumes them: K_0, then (K_j, V_{j-1}).
         for (int j = 0; j <= nbmax && ok; ++j) {
-          if (j < nbmax) ok = load_block(&tmK, j, w.bh);
-          if (ok && j >= 1) ok = load_block(&tmV, j - 1, w.bh);
+          if constexpr (C::KV_PAIRS) {
+            ok = load_pair(j, nbmax, w.bh);
+          } else {
+            if (j < nbmax) ok = load_block(&tmK, j, w.bh);
+            if (ok && j >= 1) ok = load_block(&tmV, j - 1, w.bh);
+          }
         }
       }
       // Never leave the CTA with copies in flight: wait for the last fill of
-      // every stage and of Q (already complete on the normal path).
-      for (uint32_t i = 0; i < C::STAGES && i < kv_fill; ++i) {
+      // every ring slot and of Q (already complete on the normal path).
+      for (uint32_t i = 0; i < C::RING && i < kv_fill; ++i) {
         const uint32_t f = kv_fill - 1 - i;
-        mbar_drain(BAR(C::B_KV_FULL + f % C::STAGES), (f / C::STAGES) & 1u, 100000000ull);
+        mbar_drain(BAR(C::B_KV_FULL + f % C::RING), (f / C::RING) & 1u, 100000000ull);
       }
       if (q_iter > 0) mbar_drain(BAR(C::B_Q_FULL), (q_iter - 1) & 1u, 100000000ull);
     }
@@ -378,32 +408,41 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         tc_fence_after();
         uint32_t ks = 0, vs = 0;
         if constexpr (NQ == 2) {
-          if (!(ok = next_stage(ks))) break;
+          // One wait and one release per key-block step: pair slot ps holds
+          // K_j (tile 2 ps) and V_{j-1} (tile 2 ps + 1).
+          auto next_pair = [&](uint32_t& slot) -> bool {
+            slot = kv_use % C::RING;
+            const uint32_t ph = (kv_use / C::RING) & 1u;
+            ++kv_use;
+            if (!mbar_wait(BAR(C::B_KV_FULL + slot), ph, wc, attn_internal::kStatusTimeoutMma)) return false;
+            tc_fence_after();
+            return true;
+          };
+          uint32_t ps = 0;
+          if (!(ok = next_pair(ps))) break;
           for (int t = 0; t < 2; ++t)
             if (w.nb[t] > 0) {
-              issue_qk(t, t, ks);
+              issue_qk(t, t, 2 * ps);
               mma_commit(BAR(C::B_S_FULL + t));
             }
-          mma_commit(BAR(C::B_KV_EMPTY + ks));
+          mma_commit(BAR(C::B_KV_EMPTY + ps));
           if (nbmax == 1) mma_commit(BAR(C::B_Q_EMPTY));
           for (int j = 1; j <= nbmax && ok; ++j) {
-            if (j < nbmax && !(ok = next_stage(ks))) break;
-            if (!(ok = next_stage(vs))) break;
+            if (!(ok = next_pair(ps))) break;
             for (int t = 0; t < 2 && ok; ++t) {
               if (j - 1 < w.nb[t]) {
                 if (!(ok = wait_p(t))) break;
-                issue_pv(t, t, vs, j - 1 > 0);
+                issue_pv(t, t, 2 * ps + 1, j - 1 > 0);
                 if (!C::LAST_O_DONE_ONLY || j >= w.nb[t]) mma_commit(BAR(C::B_O_DONE + t));
               }
               if (j < w.nb[t]) {
-                issue_qk(t, t, ks);
+                issue_qk(t, t, 2 * ps);
                 mma_commit(BAR(C::B_S_FULL + t));
               }
             }
             if (!ok) break;
             if (j == nbmax - 1) mma_commit(BAR(C::B_Q_EMPTY));
-            if (j < nbmax) mma_commit(BAR(C::B_KV_EMPTY + ks));
-            mma_commit(BAR(C::B_KV_EMPTY + vs));
+            mma_commit(BAR(C::B_KV_EMPTY + ps));
           }
         } else {
           const int nb = w.nb[0];
