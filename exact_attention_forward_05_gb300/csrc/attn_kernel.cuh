@@ -368,25 +368,27 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         return true;
       };
       // S[sbuf] = Q[qt] K^T   (K-major A and B, 128-byte swizzle; 32 bytes of K per MMA)
+      // Descriptors: base low word once per call, a constant offset per product.
+      constexpr uint32_t DESC_HI = desc_sw128_hi(1024);
       auto issue_qk = [&](int qt, int sbuf, uint32_t kslot) {
         const uint32_t d_tmem = tmem + (sbuf ? C::TM_S1 : C::TM_S0);
+        const uint32_t a0 = desc_sw128_lo(sQ + qt * C::TILE_BYTES, 16);
+        const uint32_t b0 = desc_sw128_lo(sKV + kslot * C::TILE_BYTES, 16);
 #pragma unroll
         for (int kk = 0; kk < C::QK_STEPS; ++kk) {
-          const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          const uint64_t a = smem_desc_sw128(sQ + qt * C::TILE_BYTES + off, 16, 1024);
-          const uint64_t b = smem_desc_sw128(sKV + kslot * C::TILE_BYTES + off, 16, 1024);
-          mma_ss(d_tmem, a, b, IDESC_QK, kk > 0 ? 1u : 0u, F8);
+          const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
+          mma_ss_w(d_tmem, a0 + off, DESC_HI, b0 + off, DESC_HI, IDESC_QK, kk > 0 ? 1u : 0u, F8);
         }
       };
       // O[ot] (+)= P[sbuf] V   (P from TMEM, V N-major in shared memory; 32 bytes of keys per MMA)
       auto issue_pv = [&](int ot, int sbuf, uint32_t vslot, bool acc) {
         const uint32_t d_tmem = tmem + (ot ? C::TM_O1 : C::TM_O0);
         const uint32_t a_tmem = tmem + (sbuf ? C::TM_S1 : C::TM_S0);
+        const uint32_t b0 = desc_sw128_lo(sKV + vslot * C::TILE_BYTES, C::CHUNK_BYTES);
 #pragma unroll
         for (int kk = 0; kk < C::PV_STEPS; ++kk) {
-          const uint64_t b = smem_desc_sw128(sKV + vslot * C::TILE_BYTES + kk * C::KSTEP * 128,
-                                             C::CHUNK_BYTES, 1024);
-          mma_ts(d_tmem, a_tmem + kk * 8, b, IDESC_PV, (acc || kk > 0) ? 1u : 0u, F8);
+          mma_ts_w(d_tmem, a_tmem + kk * 8, b0 + ((kk * C::KSTEP * 128) >> 4), DESC_HI, IDESC_PV,
+                   (acc || kk > 0) ? 1u : 0u, F8);
         }
       };
       auto wait_p = [&](int b) -> bool {
