@@ -20,7 +20,7 @@ namespace {
 
 constexpr int kHeadDim = 128;     // FP8 path: d = 128
 constexpr int kQuantRows = 128;   // rows per scale block
-constexpr int kPrepThreads = 512; // 16 warps x 8 rows each: 32 values per thread
+constexpr int kPrepThreads = 512; // 16 warps x 4 rows per pass, 2 passes: 32 values per thread
 constexpr float kE4M3Max = 448.0f;
 
 enum PrepMode : int { PREP_BLOCK = 0, PREP_AMAX = 1, PREP_QUANT_GLOBAL = 2 };
@@ -34,23 +34,40 @@ struct PrepParams {
 };
 
 // Sylvester-ordered fast Walsh-Hadamard transform of one 128-element row held
-// as 4 consecutive elements per lane (element 4*lane + e): butterflies of
-// stride 1 and 2 inside the thread, strides 4..64 across lanes.
-__device__ __forceinline__ void fwht128(float (&x)[4], int lane) {
-  const float a0 = x[0] + x[1], a1 = x[0] - x[1], a2 = x[2] + x[3], a3 = x[2] - x[3];
-  x[0] = a0 + a2;
-  x[2] = a0 - a2;
-  x[1] = a1 + a3;
-  x[3] = a1 - a3;
+// by 8 lanes (lane g of the group owns elements 16 g .. 16 g + 15): butterflies
+// of stride 1, 2, 4, 8 inside the thread, 16, 32, 64 across the group.  The
+// stages commute, so any order gives the transform.
+__device__ __forceinline__ void fwht128(float (&x)[16], int g) {
 #pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {
-    const bool upper = (lane & m) != 0;
+  for (int m = 1; m < 16; m <<= 1)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
+    for (int e = 0; e < 16; ++e)
+      if ((e & m) == 0) {
+        const float a = x[e], b = x[e + m];
+        x[e] = a + b;
+        x[e + m] = a - b;
+      }
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1) {
+    const float sgn = (g & m) ? -1.f : 1.f;  // upper half of the pair: partner - own
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
       const float o = __shfl_xor_sync(0xffffffffu, x[e], m);
-      x[e] = upper ? (o - x[e]) : (x[e] + o);
+      x[e] = fmaf(x[e], sgn, o);
     }
   }
+}
+
+// Correctly rounded x / s from y = RN(1 / s) with one FMA correction of the
+// product (Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990): q0 = RN(x y),
+// r = x - s q0 exactly, q = RN(q0 + r y).  Used where |x / s| <= 448 and s is
+// a normal number far from the exponent limits; other scales take the
+// division itself.
+__device__ __forceinline__ float div_by_scale(float x, float s, float y) {
+  const float q0 = x * y;
+  const float r = fmaf(-q0, s, x);
+  return fmaf(r, y, q0);
 }
 
 template <bool BF16IN, int MODE>
@@ -59,6 +76,7 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const PrepPar
   const int blk = blockIdx.x % p.nblk;
   const int bh = blockIdx.x / p.nblk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane & 7;                       // lane within the row's group of 8
   const bool rotate = t < 2 && p.signs != nullptr;
   const size_t head = static_cast<size_t>(bh) * p.N * kHeadDim;
   // Operands chosen by selects, not by indexing the parameter arrays (which
@@ -67,37 +85,45 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const PrepPar
   float* scale_t = t == 0 ? p.scale[0] : t == 1 ? p.scale[1] : p.scale[2];
   uint8_t* dst = t == 0 ? p.dst[0] : t == 1 ? p.dst[1] : p.dst[2];
 
-  constexpr int kWarps = kPrepThreads / 32;
-  constexpr int kRowsPerWarp = kQuantRows / kWarps;
-  float x[kRowsPerWarp][4];
+  constexpr int kRowsPerPass = kPrepThreads / 8;         // 64
+  constexpr int kPasses = kQuantRows / kRowsPerPass;      // 2
+  int rows[kPasses];
+  float x[kPasses][16];
 #pragma unroll
-  for (int i = 0; i < kRowsPerWarp; ++i) {
-    const int row = blk * kQuantRows + warp + kWarps * i;
-    if (row < p.N) {
-      const uint2 raw = *reinterpret_cast<const uint2*>(src + (head + static_cast<size_t>(row) * kHeadDim + 4 * lane) * 2);
-      if constexpr (BF16IN) {
-        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
-        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
-        x[i][0] = f0.x; x[i][1] = f0.y; x[i][2] = f1.x; x[i][3] = f1.y;
-      } else {
-        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-        x[i][0] = f0.x; x[i][1] = f0.y; x[i][2] = f1.x; x[i][3] = f1.y;
+  for (int i = 0; i < kPasses; ++i) {
+    rows[i] = blk * kQuantRows + i * kRowsPerPass + warp * 4 + (lane >> 3);
+    if (rows[i] < p.N) {
+      const uint4* ptr = reinterpret_cast<const uint4*>(
+          src + (head + static_cast<size_t>(rows[i]) * kHeadDim + 16 * g) * 2);
+      const uint4 r0 = ptr[0], r1 = ptr[1];
+      const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float2 f;
+        if constexpr (BF16IN) f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+        else f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+        x[i][2 * k] = f.x;
+        x[i][2 * k + 1] = f.y;
       }
     } else {
-      x[i][0] = x[i][1] = x[i][2] = x[i][3] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) x[i][e] = 0.f;
     }
   }
   if (rotate) {
-    const int8_t* sg = p.signs + (bh % p.H) * kHeadDim + 4 * lane;
-    const float s0 = sg[0], s1 = sg[1], s2 = sg[2], s3 = sg[3];
+    const int4 sg = *reinterpret_cast<const int4*>(p.signs + (bh % p.H) * kHeadDim + 16 * g);
+    const int sw[4] = {sg.x, sg.y, sg.z, sg.w};
     const float inv_sqrt_d = 0.08838834764831845f;  // 1 / sqrt(128)
 #pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) {
-      x[i][0] *= s0; x[i][1] *= s1; x[i][2] *= s2; x[i][3] *= s3;
-      fwht128(x[i], lane);
+    for (int i = 0; i < kPasses; ++i) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) x[i][e] *= inv_sqrt_d;
+      for (int e = 0; e < 16; ++e) {
+        const int sb = static_cast<int8_t>((sw[e >> 2] >> (8 * (e & 3))) & 0xff);
+        x[i][e] *= static_cast<float>(sb);
+      }
+      fwht128(x[i], g);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) x[i][e] *= inv_sqrt_d;
     }
   }
 
@@ -105,9 +131,9 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const PrepPar
   __shared__ float warp_max[kPrepThreads / 32];
   float a = 0.f;
 #pragma unroll
-  for (int i = 0; i < kRowsPerWarp; ++i)
+  for (int i = 0; i < kPasses; ++i)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) a = fmaxf(a, fabsf(x[i][e]));
+    for (int e = 0; e < 16; ++e) a = fmaxf(a, fabsf(x[i][e]));
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
   if (lane == 0) warp_max[warp] = a;
@@ -125,18 +151,28 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const PrepPar
       s = amax > 0.f ? amax / kE4M3Max : 1.f;
       if (threadIdx.x == 0) scale_t[static_cast<size_t>(bh) * p.nblk + blk] = s;
     } else {
-      const float g = __uint_as_float(*reinterpret_cast<const unsigned int*>(scale_t));
-      s = g > 0.f ? g / kE4M3Max : 1.f;
+      const float g_amax = __uint_as_float(*reinterpret_cast<const unsigned int*>(scale_t));
+      s = g_amax > 0.f ? g_amax / kE4M3Max : 1.f;
     }
+    // Block-uniform choice: the FMA-corrected quotient for ordinary scales.
+    const bool fast = s >= 0x1p-100f && s <= 0x1p+100f;
+    const float y = __frcp_rn(s);
 #pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) {
-      const int row = blk * kQuantRows + warp + kWarps * i;
-      if (row >= p.N) continue;
-      const uint32_t lo = __nv_cvt_float2_to_fp8x2(
-          make_float2(__fdiv_rn(x[i][0], s), __fdiv_rn(x[i][1], s)), __NV_SATFINITE, __NV_E4M3);
-      const uint32_t hi = __nv_cvt_float2_to_fp8x2(
-          make_float2(__fdiv_rn(x[i][2], s), __fdiv_rn(x[i][3], s)), __NV_SATFINITE, __NV_E4M3);
-      *reinterpret_cast<uint32_t*>(dst + head + static_cast<size_t>(row) * kHeadDim + 4 * lane) = lo | (hi << 16);
+    for (int i = 0; i < kPasses; ++i) {
+      if (rows[i] >= p.N) continue;
+      uint32_t pk[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float q[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          q[e] = fast ? div_by_scale(x[i][4 * k + e], s, y) : __fdiv_rn(x[i][4 * k + e], s);
+        const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(q[0], q[1]), __NV_SATFINITE, __NV_E4M3);
+        const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(q[2], q[3]), __NV_SATFINITE, __NV_E4M3);
+        pk[k] = lo | (hi << 16);
+      }
+      *reinterpret_cast<uint4*>(dst + head + static_cast<size_t>(rows[i]) * kHeadDim + 16 * g) =
+          make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
   }
 }
@@ -194,6 +230,7 @@ ATTN_EXPORT attn_status attn_fp8_prepare(const void* q, const void* k, const voi
       !aligned(v8, 16))
     return ATTN_ERR_MISALIGNED;
   if (!aligned(q_scale, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4)) return ATTN_ERR_MISALIGNED;
+  if (signs && !aligned(signs, 16)) return ATTN_ERR_MISALIGNED;  // read 16 signs per load
   PrepParams prm;
   prm.src[0] = q; prm.src[1] = k; prm.src[2] = v;
   prm.dst[0] = static_cast<uint8_t*>(q8);

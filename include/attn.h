@@ -137,7 +137,8 @@ attn_status attn_fwd_host_noalloc(const void* q_host, const void* k_host, const 
  *   q_scale, k_scale, v_scale : device float32, written.  Per-block mode:
  *                 [B, H, ceil(N/128)], one scale per 128 rows of a head.
  *                 Per-tensor mode: one float each.
- *   signs       : [H, d] device int8, +1 / -1; NULL = no rotation.  With signs,
+ *   signs       : [H, d] device int8, +1 / -1, 16-byte aligned (else
+ *                 ATTN_ERR_MISALIGNED); NULL = no rotation.  With signs,
  *                 every row x of Q and K (head h) is replaced by
  *                 (x * signs[h]) H_d / sqrt(d), H_d the Sylvester Hadamard
  *                 matrix (an orthogonal map shared by Q and K, so Q K^T is

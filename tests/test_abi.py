@@ -86,10 +86,10 @@ def test_fp8_validation_before_launch(lib):
     args = dict(q=0x1000, k=0x2000, v=0x3000, q8=0x4000, k8=0x5000, v8=0x6000, qs=0x7000,
                 ks=0x8000, vs=0x9000)
 
-    def prep(d=128, dtype=attn.ATTN_BF16, N=64, **kw):
+    def prep(d=128, dtype=attn.ATTN_BF16, N=64, signs=None, **kw):
         a = dict(args, **kw)
         return lib.attn_fp8_prepare(a["q"], a["k"], a["v"], dtype, a["q8"], a["k8"], a["v8"],
-                                    a["qs"], a["ks"], a["vs"], None, 0, 1, 2, N, d, None)
+                                    a["qs"], a["ks"], a["vs"], signs, 0, 1, 2, N, d, None)
 
     def fwd(d=128, N=64, scale=0.1, **kw):
         a = dict(args, o=0xA000, lse=0xB000)
@@ -103,6 +103,7 @@ def test_fp8_validation_before_launch(lib):
     assert prep(ks=None) == attn.ATTN_ERR_INVALID_ARG
     assert prep(k=0x2004) == attn.ATTN_ERR_MISALIGNED
     assert prep(vs=0x9002) == attn.ATTN_ERR_MISALIGNED
+    assert prep(signs=0xC008) == attn.ATTN_ERR_MISALIGNED
     assert prep(N=0) == attn.ATTN_OK
     assert fwd(d=256) == attn.ATTN_ERR_UNSUPPORTED
     assert fwd(scale=float("nan")) == attn.ATTN_ERR_INVALID_ARG
