@@ -20,7 +20,7 @@ namespace {
 
 constexpr int kHeadDim = 128;     // FP8 path: d = 128
 constexpr int kQuantRows = 128;   // rows per scale block
-constexpr int kPrepThreads = 512; // 16 warps x 4 rows per pass, 2 passes: 32 values per thread
+constexpr int kPrepThreads = 512; // 16 warps x 8 rows, 4 lanes x 32 values per row
 constexpr float kE4M3Max = 448.0f;
 
 enum PrepMode : int { PREP_BLOCK = 0, PREP_AMAX = 1, PREP_QUANT_GLOBAL = 2 };
@@ -34,24 +34,24 @@ struct PrepParams {
 };
 
 // Sylvester-ordered fast Walsh-Hadamard transform of one 128-element row held
-// by 8 lanes (lane g of the group owns elements 16 g .. 16 g + 15): butterflies
-// of stride 1, 2, 4, 8 inside the thread, 16, 32, 64 across the group.  The
-// stages commute, so any order gives the transform.
-__device__ __forceinline__ void fwht128(float (&x)[16], int g) {
+// by 4 lanes (lane g of the group owns elements 32 g .. 32 g + 31): butterflies
+// of stride 1 .. 16 inside the thread, 32 and 64 across the group.  The stages
+// commute, so any order gives the transform.
+__device__ __forceinline__ void fwht128(float (&x)[32], int g) {
 #pragma unroll
-  for (int m = 1; m < 16; m <<= 1)
+  for (int m = 1; m < 32; m <<= 1)
 #pragma unroll
-    for (int e = 0; e < 16; ++e)
+    for (int e = 0; e < 32; ++e)
       if ((e & m) == 0) {
         const float a = x[e], b = x[e + m];
         x[e] = a + b;
         x[e + m] = a - b;
       }
 #pragma unroll
-  for (int m = 1; m < 8; m <<= 1) {
+  for (int m = 1; m < 4; m <<= 1) {
     const float sgn = (g & m) ? -1.f : 1.f;  // upper half of the pair: partner - own
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
+    for (int e = 0; e < 32; ++e) {
       const float o = __shfl_xor_sync(0xffffffffu, x[e], m);
       x[e] = fmaf(x[e], sgn, o);
     }
@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const PrepPar
   const int blk = blockIdx.x % p.nblk;
   const int bh = blockIdx.x / p.nblk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane & 7;                       // lane within the row's group of 8
+  const int g = lane & 3;                       // lane within the row's group of 4
   const bool rotate = t < 2 && p.signs != nullptr;
   const size_t head = static_cast<size_t>(bh) * p.N * kHeadDim;
   // Operands chosen by selects, not by indexing the parameter arrays (which
@@ -85,55 +85,52 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const PrepPar
   float* scale_t = t == 0 ? p.scale[0] : t == 1 ? p.scale[1] : p.scale[2];
   uint8_t* dst = t == 0 ? p.dst[0] : t == 1 ? p.dst[1] : p.dst[2];
 
-  constexpr int kRowsPerPass = kPrepThreads / 8;         // 64
-  constexpr int kPasses = kQuantRows / kRowsPerPass;      // 2
-  int rows[kPasses];
-  float x[kPasses][16];
+  const int row = blk * kQuantRows + warp * 8 + (lane >> 2);
+  float x[32];
+  if (row < p.N) {
+    const uint4* ptr = reinterpret_cast<const uint4*>(
+        src + (head + static_cast<size_t>(row) * kHeadDim + 32 * g) * 2);
 #pragma unroll
-  for (int i = 0; i < kPasses; ++i) {
-    rows[i] = blk * kQuantRows + i * kRowsPerPass + warp * 4 + (lane >> 3);
-    if (rows[i] < p.N) {
-      const uint4* ptr = reinterpret_cast<const uint4*>(
-          src + (head + static_cast<size_t>(rows[i]) * kHeadDim + 16 * g) * 2);
-      const uint4 r0 = ptr[0], r1 = ptr[1];
-      const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+    for (int v = 0; v < 4; ++v) {
+      const uint4 r = ptr[v];
+      const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < 4; ++k) {
         float2 f;
         if constexpr (BF16IN) f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
         else f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
-        x[i][2 * k] = f.x;
-        x[i][2 * k + 1] = f.y;
+        x[8 * v + 2 * k] = f.x;
+        x[8 * v + 2 * k + 1] = f.y;
       }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 16; ++e) x[i][e] = 0.f;
     }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) x[e] = 0.f;
   }
   if (rotate) {
-    const int4 sg = *reinterpret_cast<const int4*>(p.signs + (bh % p.H) * kHeadDim + 16 * g);
-    const int sw[4] = {sg.x, sg.y, sg.z, sg.w};
+    // Signs (+1 = 0x01, -1 = 0xff): bit 7 of each byte becomes the float's sign bit.
+    const int4* sp = reinterpret_cast<const int4*>(p.signs + (bh % p.H) * kHeadDim + 32 * g);
+    const int4 s0 = sp[0], s1 = sp[1];
+    const uint32_t sw[8] = {static_cast<uint32_t>(s0.x), static_cast<uint32_t>(s0.y),
+                            static_cast<uint32_t>(s0.z), static_cast<uint32_t>(s0.w),
+                            static_cast<uint32_t>(s1.x), static_cast<uint32_t>(s1.y),
+                            static_cast<uint32_t>(s1.z), static_cast<uint32_t>(s1.w)};
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const uint32_t bit = (sw[e >> 2] << (24 - 8 * (e & 3))) & 0x80000000u;
+      x[e] = __uint_as_float(__float_as_uint(x[e]) ^ bit);
+    }
+    fwht128(x, g);
     const float inv_sqrt_d = 0.08838834764831845f;  // 1 / sqrt(128)
 #pragma unroll
-    for (int i = 0; i < kPasses; ++i) {
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int sb = static_cast<int8_t>((sw[e >> 2] >> (8 * (e & 3))) & 0xff);
-        x[i][e] *= static_cast<float>(sb);
-      }
-      fwht128(x[i], g);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) x[i][e] *= inv_sqrt_d;
-    }
+    for (int e = 0; e < 32; ++e) x[e] *= inv_sqrt_d;
   }
 
   // amax of the block
   __shared__ float warp_max[kPrepThreads / 32];
   float a = 0.f;
 #pragma unroll
-  for (int i = 0; i < kPasses; ++i)
-#pragma unroll
-    for (int e = 0; e < 16; ++e) a = fmaxf(a, fabsf(x[i][e]));
+  for (int e = 0; e < 32; ++e) a = fmaxf(a, fabsf(x[e]));
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
   if (lane == 0) warp_max[warp] = a;
@@ -157,22 +154,21 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const PrepPar
     // Block-uniform choice: the FMA-corrected quotient for ordinary scales.
     const bool fast = s >= 0x1p-100f && s <= 0x1p+100f;
     const float y = __frcp_rn(s);
+    if (row < p.N) {
+      uint32_t pk[8];
 #pragma unroll
-    for (int i = 0; i < kPasses; ++i) {
-      if (rows[i] >= p.N) continue;
-      uint32_t pk[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < 8; ++k) {
         float q[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          q[e] = fast ? div_by_scale(x[i][4 * k + e], s, y) : __fdiv_rn(x[i][4 * k + e], s);
+          q[e] = fast ? div_by_scale(x[4 * k + e], s, y) : __fdiv_rn(x[4 * k + e], s);
         const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(q[0], q[1]), __NV_SATFINITE, __NV_E4M3);
         const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(q[2], q[3]), __NV_SATFINITE, __NV_E4M3);
         pk[k] = lo | (hi << 16);
       }
-      *reinterpret_cast<uint4*>(dst + head + static_cast<size_t>(rows[i]) * kHeadDim + 16 * g) =
-          make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      uint4* out = reinterpret_cast<uint4*>(dst + head + static_cast<size_t>(row) * kHeadDim + 32 * g);
+      out[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      out[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
     }
   }
 }
