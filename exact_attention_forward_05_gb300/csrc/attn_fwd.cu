@@ -79,6 +79,42 @@ ATTN_EXPORT attn_status attn_fwd(const void* q, const void* k, const void* v, vo
   }
 }
 
+namespace {
+
+// Streams and events of the host-buffer pipeline, created once per device.
+constexpr int kHostChunks = 8;
+struct HostPipe {
+  std::mutex mu;
+  cudaStream_t st[3];  // copies in, kernels, copies out
+  cudaEvent_t start;
+  cudaEvent_t in[kHostChunks], done[kHostChunks];
+};
+
+attn_status host_pipe(HostPipe** out) {
+  static std::mutex mu;
+  static HostPipe* pipes[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return attn_internal::cuda_status(e);
+  if (dev < 0 || dev >= 64) return ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(mu);
+  if (pipes[dev] == nullptr) {
+    HostPipe* hp = new HostPipe();
+    bool good = true;
+    for (int i = 0; i < 3 && good; ++i) good = cudaStreamCreateWithFlags(&hp->st[i], cudaStreamNonBlocking) == cudaSuccess;
+    good = good && cudaEventCreateWithFlags(&hp->start, cudaEventDisableTiming) == cudaSuccess;
+    for (int c = 0; c < kHostChunks && good; ++c)
+      good = cudaEventCreateWithFlags(&hp->in[c], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&hp->done[c], cudaEventDisableTiming) == cudaSuccess;
+    if (!good) return attn_internal::cuda_status(cudaGetLastError());  // kept for the process (not freed)
+    pipes[dev] = hp;
+  }
+  *out = pipes[dev];
+  return ATTN_OK;
+}
+
+}  // namespace
+
 ATTN_EXPORT size_t attn_fwd_host_workspace_bytes(int B, int H, int N, int d, attn_dtype dtype) {
   (void)dtype;
   if (B < 0 || H < 0 || N < 0 || d <= 0) return 0;
@@ -97,25 +133,59 @@ ATTN_EXPORT attn_status attn_fwd_host(const void* q_host, const void* k_host, co
   if (!attn_internal::aligned(workspace, 256)) return ATTN_ERR_MISALIGNED;
   const size_t bytes = static_cast<size_t>(B) * H * N * d * 2;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  void* dq = ws;
-  void* dk = ws + align256(bytes);
-  void* dv = ws + 2 * align256(bytes);
-  void* dout = ws + 3 * align256(bytes);
+  uint8_t* dq = ws;
+  uint8_t* dk = ws + align256(bytes);
+  uint8_t* dv = ws + 2 * align256(bytes);
+  uint8_t* dout = ws + 3 * align256(bytes);
   float* dlse = reinterpret_cast<float*>(ws + 4 * align256(bytes));
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if ((e = cudaMemcpyAsync(dq, q_host, bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
-      (e = cudaMemcpyAsync(dk, k_host, bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
-      (e = cudaMemcpyAsync(dv, v_host, bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
-    return attn_internal::cuda_status(e);
-  st = attn_fwd(dq, dk, dv, dout, lse_host ? dlse : nullptr, B, H, N, d, causal, scale, dtype, stream);
+  const uint8_t* hq = static_cast<const uint8_t*>(q_host);
+  const uint8_t* hk = static_cast<const uint8_t*>(k_host);
+  const uint8_t* hv = static_cast<const uint8_t*>(v_host);
+  uint8_t* ho = static_cast<uint8_t*>(o_host);
+
+  // Pipeline over chunks of consecutive (batch, head) pairs, contiguous in
+  // every tensor: chunk c's inputs are copied in on one stream while the
+  // kernel runs on chunk c - 1 on a second and chunk c - 2's output is copied
+  // out on a third, so copies in both directions overlap the compute.
+  HostPipe* hp = nullptr;
+  st = host_pipe(&hp);
   if (st != ATTN_OK) return st;
-  if ((e = cudaMemcpyAsync(o_host, dout, bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
-    return attn_internal::cuda_status(e);
-  if (lse_host &&
-      (e = cudaMemcpyAsync(lse_host, dlse, static_cast<size_t>(B) * H * N * 4, cudaMemcpyDeviceToHost, s)) !=
-          cudaSuccess)
-    return attn_internal::cuda_status(e);
+  std::lock_guard<std::mutex> lock(hp->mu);  // the streams and events serve one call at a time
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int BH = B * H;
+  const int nchunk = BH < kHostChunks ? BH : kHostChunks;
+  const size_t row_bytes = static_cast<size_t>(N) * d * 2;  // one (batch, head) of Q/K/V/O
+  cudaError_t e;
+  // Work already queued on the caller's stream comes first.
+  if ((e = cudaEventRecord(hp->start, s)) != cudaSuccess) return attn_internal::cuda_status(e);
+  for (int i = 0; i < 3; ++i)
+    if ((e = cudaStreamWaitEvent(hp->st[i], hp->start, 0)) != cudaSuccess) return attn_internal::cuda_status(e);
+  for (int c = 0; c < nchunk; ++c) {
+    const int bh0 = static_cast<int>(static_cast<int64_t>(BH) * c / nchunk);
+    const int bh1 = static_cast<int>(static_cast<int64_t>(BH) * (c + 1) / nchunk);
+    const size_t off = row_bytes * bh0, len = row_bytes * (bh1 - bh0);
+    if ((e = cudaMemcpyAsync(dq + off, hq + off, len, cudaMemcpyHostToDevice, hp->st[0])) != cudaSuccess ||
+        (e = cudaMemcpyAsync(dk + off, hk + off, len, cudaMemcpyHostToDevice, hp->st[0])) != cudaSuccess ||
+        (e = cudaMemcpyAsync(dv + off, hv + off, len, cudaMemcpyHostToDevice, hp->st[0])) != cudaSuccess ||
+        (e = cudaEventRecord(hp->in[c], hp->st[0])) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(hp->st[1], hp->in[c], 0)) != cudaSuccess)
+      return attn_internal::cuda_status(e);
+    st = attn_fwd(dq + off, dk + off, dv + off, dout + off,
+                  lse_host ? dlse + static_cast<size_t>(N) * bh0 : nullptr, 1, bh1 - bh0, N, d, causal,
+                  scale, dtype, hp->st[1]);
+    if (st != ATTN_OK) return st;
+    if ((e = cudaEventRecord(hp->done[c], hp->st[1])) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(hp->st[2], hp->done[c], 0)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(ho + off, dout + off, len, cudaMemcpyDeviceToHost, hp->st[2])) != cudaSuccess)
+      return attn_internal::cuda_status(e);
+    if (lse_host &&
+        (e = cudaMemcpyAsync(lse_host + static_cast<size_t>(N) * bh0, dlse + static_cast<size_t>(N) * bh0,
+                             static_cast<size_t>(N) * (bh1 - bh0) * 4, cudaMemcpyDeviceToHost, hp->st[2])) !=
+            cudaSuccess)
+      return attn_internal::cuda_status(e);
+  }
+  for (int i = 0; i < 3; ++i)
+    if ((e = cudaStreamSynchronize(hp->st[i])) != cudaSuccess) return attn_internal::cuda_status(e);
   return attn_internal::cuda_status(cudaStreamSynchronize(s));
 }
 
