@@ -116,7 +116,11 @@ struct Cfg {
   // Shared memory layout (offsets from a 1024-byte aligned base).
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = NQ * TILE_BYTES;
-  static constexpr int OFF_BAR = OFF_KV + STAGES * TILE_BYTES;
+  // O staging for the bulk tensor store: per Q tile one 128-byte column span
+  // of the 16-bit output (128 rows x 64 columns), 128-byte swizzled.
+  static constexpr int OST_BYTES = kBM * 128;
+  static constexpr int OFF_OST = OFF_KV + STAGES * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_OST + NQ * OST_BYTES;
   static constexpr int SMEM_BYTES = OFF_BAR + 8 * NBARS + 16 + 1024;
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(SMEM_BYTES > 114 * 1024, "one CTA per SM (TMEM is allocated whole)");
@@ -216,7 +220,8 @@ __device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, uint64
 template <int D, int KIND>
 __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const FwdParams p) {
   using C = Cfg<D, KIND>;
   constexpr int NQ = C::NQ;
   constexpr bool F8 = KIND == KIND_E4M3;
@@ -653,38 +658,64 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(C::B_P_FULL + b));
       }
-      if (!ok) break;
+      // A failed wait above (ok = false) still leads to the tile barrier below,
+      // where the four warps leave together.
 
-      // Epilogue: O / l (times svmax for FP8), rounded to the output dtype; lse.
-      if (!(ok = mbar_wait_warp(BAR(C::B_O_DONE + wg), oph, wc, attn_internal::kStatusTimeoutSoftmax))) break;
+      // Epilogue: O / l (times svmax for FP8), rounded to the output dtype, and
+      // lse.  O leaves through this tile's staging buffer, 64 columns at a
+      // time, by a bulk tensor store (rows past N are not written).  The four
+      // warps of the tile first agree that every one of them saw O_DONE, so
+      // that none waits at a tile barrier another has left.
+      const bool got_o = ok && mbar_wait_warp(BAR(C::B_O_DONE + wg), oph, wc, attn_internal::kStatusTimeoutSoftmax);
+      const uint32_t tile_bar = 1u + static_cast<uint32_t>(wg);
+      if (bar_red_or(tile_bar, 128, !got_o)) {
+        ok = false;
+        break;
+      }
       oph ^= 1u;
       tc_fence_after();
       const float inv_l = sv_max / l;
-      const bool store = qi < p.N;
-      uint8_t* orow = static_cast<uint8_t*>(p.o) +
-                      (static_cast<size_t>(w.bh) * p.N + (store ? qi : 0)) * D * 2;
+      const uint32_t ost = smem_u32(smem + C::OFF_OST + wg * C::OST_BYTES);
+      const uint32_t ost_row = ost + static_cast<uint32_t>(row) * 128u;
+      const uint32_t swz = static_cast<uint32_t>(row & 7);
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tm_o + 32 * c, o);
-        tmem_wait_ld(o);
-        uint32_t pk[16];
+      for (int c2 = 0; c2 < D / 64; ++c2) {
+        uint32_t o[2][32];
+        tmem_ld32(tm_o + 64 * c2, o[0]);
+        tmem_ld32(tm_o + 64 * c2 + 32, o[1]);
+        tmem_wait_ld(o[0]);
+        reg_pin(o[1]);
+        // The previous bulk store from this buffer must have read it.
+        if (wq == 0 && lane == 0) bulk_wait_read_all();
+        bar_sync_n(tile_bar, 128);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack2<F8 ? KIND_BF16 : KIND>(__uint_as_float(o[2 * i]) * inv_l,
-                                               __uint_as_float(o[2 * i + 1]) * inv_l);
-        if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[16];
 #pragma unroll
-          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack2<F8 ? KIND_BF16 : KIND>(__uint_as_float(o[h][2 * i]) * inv_l,
+                                                 __uint_as_float(o[h][2 * i + 1]) * inv_l);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint32_t unit = static_cast<uint32_t>(4 * h + v);
+            st_shared_v4(ost_row + ((unit ^ swz) << 4), pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+        bar_sync_n(tile_bar, 128);
+        if (wq == 0 && lane == 0) {
+          tma_store_3d(&tmO, ost, 64 * c2, tile_row0, w.bh);
+          bulk_commit_group();
         }
       }
-      if (store && p.lse != nullptr)
+      if (qi < p.N && p.lse != nullptr)
         p.lse[static_cast<size_t>(w.bh) * p.N + qi] = (m_used + log2f(l)) * 0.69314718055994531f;
       tc_fence_before();
     }
   }
 
+  // The bulk stores of O read shared memory: let them finish before the CTA exits.
+  if (warp < C::SOFTMAX_WARPS && (warp & 3) == 0 && lane == 0) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == C::MMA_WARP) {
@@ -704,10 +735,12 @@ attn_status launch_fwd(const void* q, const void* k, const void* v, FwdParams pr
                                  : KIND == KIND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const uint64_t BH = static_cast<uint64_t>(B) * H;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
+  const CUtensorMapDataType dto = KIND == KIND_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (!attn_internal::encode_tmap_3d(&mq, dt, q, D, N, BH, C::ELEM, C::CHUNK_ELEMS, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !attn_internal::encode_tmap_3d(&mk, dt, k, D, N, BH, C::ELEM, C::CHUNK_ELEMS, kBN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !attn_internal::encode_tmap_3d(&mv, dt, v, D, N, BH, C::ELEM, C::CHUNK_ELEMS, kBN, CU_TENSOR_MAP_SWIZZLE_128B))
+      !attn_internal::encode_tmap_3d(&mv, dt, v, D, N, BH, C::ELEM, C::CHUNK_ELEMS, kBN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !attn_internal::encode_tmap_3d(&mo, dto, prm.o, D, N, BH, 2, 64, kBM, CU_TENSOR_MAP_SWIZZLE_128B))
     return ATTN_ERR_CUDA;
 
   static int configured_for[64] = {0};  // per device: dynamic shared memory attribute set
@@ -744,7 +777,7 @@ attn_status launch_fwd(const void* q, const void* k, const void* v, FwdParams pr
     }
   }
   const int grid = prm.num_units < sms ? prm.num_units : sms;
-  attn_fwd_kernel<D, KIND><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, prm);
+  attn_fwd_kernel<D, KIND><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mo, prm);
   return attn_internal::cuda_status(cudaGetLastError());
 }
 
