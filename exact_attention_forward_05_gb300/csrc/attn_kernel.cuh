@@ -9,12 +9,19 @@
 //   softmax group t (4 warps per Q tile): thread = one query row = one TMEM
 //       lane.  Loads its row of S from TMEM, runs the online softmax, writes P
 //       back over S, rescales O when needed, and at the end divides O by the
-//       running sum and stores O and lse.
+//       running sum and writes O (through shared memory and a bulk tensor
+//       store) and lse.
 //   load warp: TMA loads of Q (once per unit) and of K_j / V_j blocks into a
-//       ring of shared-memory stages guarded by mbarriers.
+//       ring of shared-memory stages guarded by mbarriers (two Q tiles: K_j and
+//       V_{j-1} share one ring slot with one full and one empty barrier).
 //   MMA warp: one thread issues tcgen05.mma: S = Q K_j^T (both operands in
 //       shared memory) and O += P V_j (P read from TMEM, V from shared memory),
 //       accumulating in TMEM, and signals completion with tcgen05.commit.
+//       Every instruction of this thread is on the critical path (one
+//       tcgen05.mma takes about as long to issue as a 128x128x16 product takes
+//       to run), so its waits, commits and descriptor arithmetic are kept few.
+// Two Q tiles: 12 warps = 3 warpgroups; the third (load, MMA, 2 idle warps)
+// hands registers to the two softmax warpgroups with setmaxnreg.
 //
 // The pages' method: tiles of Q, K, V moved to on-chip memory, the softmax
 // computed blockwise with a running maximum and a separately tracked running
