@@ -457,8 +457,9 @@ def run_reference(args):
 
 def run_sweep(args):
     """One device-timed line per point of the sequence-length sweep (bf16,
-    B = 16384/N, H = 2048/d, causal and non-causal), and the FP8 kernel at
-    d = 128 (H = 16, inputs with 0.1 % outliers).  Same timing as the main
+    B = 16384/N, H = 2048/d, causal and non-causal), the FP8 kernel at
+    d = 128 (H = 16, inputs with 0.1 % outliers), and the long-context causal
+    case (B = 1, H = 16, N = 32768, d = 128).  Same timing as the main
     line: CUDA events on the launching stream around ``--steps`` launches."""
     import exact_attention_forward_05_gb300 as attn
     import synth
@@ -492,6 +493,15 @@ def run_sweep(args):
                                           return_lse=False, stream=stream)
             emit(dict(B=B, H=H, N=N, d=d, causal=causal, dtype="fp8 e4m3"),
                  time_kernel(f, args.steps, args.warmup, stream) / args.steps, 2 * peak)
+    # Long-context configuration: B = 1, H = 16, N = 32768, d = 128, causal.
+    B, H, N, d = 1, 16, 32768, 128
+    q, k, v = (t.to(dev) for t in synth.attention_inputs(B, H, N, d, "bf16", seed=0))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    f = lambda: attn.attn_fwd(q, k, v, causal=True, scale=d ** -0.5, out=o, lse=lse, stream=stream)
+    emit(dict(B=B, H=H, N=N, d=d, causal=True, dtype="bf16"),
+         time_kernel(f, args.steps, args.warmup, stream) / args.steps, peak)
+    del q, k, v, o, lse
     if attn.device_status() != attn.ATTN_OK:
         raise RuntimeError("device status after the sweep")
 
