@@ -97,11 +97,11 @@ struct Cfg {
   static constexpr bool KV_PAIRS = NQ == 2;
   static constexpr int RING = KV_PAIRS ? STAGES / 2 : STAGES;
   static constexpr int SOFTMAX_WARPS = 4 * NQ;
-  // Two Q tiles, E4M3: the products P_{j-1} V_{j-1} signal nothing of their
-  // own; the softmax learns of their completion from the S_FULL commit of the
-  // next Q K^T, which is issued after them (only the tile's last product
-  // signals O_DONE).  Measured faster for E4M3 and not for 16-bit operands.
-  static constexpr bool LAST_O_DONE_ONLY = NQ == 2 && KIND == KIND_E4M3;
+  // Two Q tiles: the products P_{j-1} V_{j-1} signal nothing of their own;
+  // the softmax learns of their completion from the S_FULL commit of the next
+  // Q K^T, which is issued after them (only the tile's last product signals
+  // O_DONE), which saves the MMA-issuing thread two commits per key block.
+  static constexpr bool LAST_O_DONE_ONLY = NQ == 2;
   static constexpr int LOAD_WARP = SOFTMAX_WARPS;
   static constexpr int MMA_WARP = SOFTMAX_WARPS + 1;
   // Two Q tiles: three whole warpgroups (softmax, softmax, load + MMA + two
