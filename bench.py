@@ -455,6 +455,48 @@ def run_reference(args):
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_ablation(args):
+    """Overlap ablation (in the spirit of the FlashAttention-3 page's ablation
+    table): the bench workload, causal and not, and the FP8 kernel, timed with
+    two Q tiles per CTA whose softmax and products overlap (ping-pong, the
+    default) and with one Q tile per CTA at a time (no overlap)."""
+    import exact_attention_forward_05_gb300 as attn
+    import synth
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    peak = peaks()[0]
+    B, H, N, d = 2, 16, 8192, 128
+    q, k, v = (t.to(dev) for t in synth.attention_inputs(B, H, N, d, "bf16", seed=0))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    qo, ko, vo = (t.to(dev) for t in synth.outlier_inputs(B, H, N, d, "bf16", seed=0))
+    bufs = attn.fp8_prepare(qo, ko, vo, signs=synth.hadamard_signs(H, d, seed=0).to(dev))
+    o8 = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    try:
+        for mode, name in ((attn.SCHEDULE_PINGPONG, "ping-pong (two Q tiles, overlap)"),
+                           (attn.SCHEDULE_ONE_TILE, "one Q tile per CTA (no overlap)")):
+            attn.set_schedule(mode)
+            for causal in (False, True):
+                f = lambda: attn.attn_fwd(q, k, v, causal=causal, scale=d ** -0.5, out=o, lse=lse,
+                                          stream=stream)
+                w = dict(B=B, H=H, N=N, d=d, causal=causal, dtype="bf16")
+                ms = time_kernel(f, args.steps, args.warmup, stream) / args.steps
+                tf = flops(w) / (ms * 1e-3) / 1e12
+                print(json.dumps({"schedule": name, "workload": describe(w), "value": round(tf, 1),
+                                  "unit": UNIT, "frac": round(tf / peak, 4), "ms": round(ms, 4)}), flush=True)
+            f = lambda: attn.attn_fwd_fp8(*bufs, causal=False, scale=d ** -0.5, out=o8,
+                                          return_lse=False, stream=stream)
+            w = dict(B=B, H=H, N=N, d=d, causal=False, dtype="fp8 e4m3")
+            ms = time_kernel(f, args.steps, args.warmup, stream) / args.steps
+            tf = flops(w) / (ms * 1e-3) / 1e12
+            print(json.dumps({"schedule": name, "workload": describe(w), "value": round(tf, 1),
+                              "unit": UNIT, "frac": round(tf / (2 * peak), 4), "ms": round(ms, 4)}), flush=True)
+    finally:
+        attn.set_schedule(attn.SCHEDULE_PINGPONG)
+    if attn.device_status() != attn.ATTN_OK:
+        raise RuntimeError("device status after the ablation")
+
+
 def run_sweep(args):
     """One device-timed line per point of the sequence-length sweep (bf16,
     B = 16384/N, H = 2048/d, causal and non-causal), the FP8 kernel at
@@ -513,11 +555,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--ablation", action="store_true",
+                    help="overlap ablation: the bench workload under both work schedules, one line each")
     ap.add_argument("--sweep", action="store_true",
                     help="print one device-timed line per sweep configuration instead")
     args = ap.parse_args()
     if args.sweep:
         run_sweep(args)
+        return
+    if args.ablation:
+        run_ablation(args)
         return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -22,7 +22,7 @@ import torch
 from . import build as _build
 
 __all__ = ["attn_fwd", "attn_fwd_host", "fp8_prepare", "attn_fwd_fp8", "attn_fwd_fp8_pipeline", "host_workspace_bytes", "device_status",
-           "set_wait_timeout_ns", "debug_bounded_wait", "status_string", "library_path",
+           "set_wait_timeout_ns", "set_schedule", "debug_bounded_wait", "status_string", "library_path",
            "AttnError", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
            "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "exported_symbols"]
 
@@ -73,6 +73,7 @@ def _load():
             lib.attn_get_device_status.restype = i32
             lib.attn_set_wait_timeout_ns.argtypes = [u64]
             lib.attn_set_wait_timeout_ns.restype = None
+            lib.attn_set_schedule.argtypes = [i32]
             lib.attn_debug_bounded_wait.argtypes = [u64, vp]
             lib.attn_debug_bounded_wait.restype = i32
             lib.attn_last_cuda_error.argtypes = []
@@ -267,6 +268,16 @@ def device_status(stream=None) -> int:
 
 def set_wait_timeout_ns(ns: int) -> None:
     _load().attn_set_wait_timeout_ns(int(ns))
+
+
+SCHEDULE_PINGPONG, SCHEDULE_ONE_TILE = 0, 1
+
+
+def set_schedule(mode: int) -> None:
+    """Work schedule of later launches with d <= 128: SCHEDULE_PINGPONG (two Q
+    tiles per CTA, softmax of one overlapping the products of the other; the
+    default) or SCHEDULE_ONE_TILE (one tile at a time, the overlap ablation)."""
+    _check(_load().attn_set_schedule(int(mode)), "attn_set_schedule")
 
 
 def debug_bounded_wait(timeout_ns: int, stream=None) -> None:

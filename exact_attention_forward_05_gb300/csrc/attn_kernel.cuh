@@ -773,7 +773,10 @@ attn_status launch_fwd(const void* q, const void* k, const void* v, FwdParams pr
   // half units (one Q tile each, one per CTA), so that round costs half a unit.
   prm.full_units = units;
   prm.num_units = units;
-  if (C::NQ == 2 && !prm.causal) {
+  if (C::NQ == 2 && attn_internal::schedule_mode() == ATTN_SCHEDULE_ONE_TILE) {
+    prm.full_units = 0;  // every entry a half unit: one Q tile per CTA at a time
+    prm.num_units = 2 * units;
+  } else if (C::NQ == 2 && !prm.causal) {
     const int rest = units % sms;
     if (units <= sms / 2) {
       prm.full_units = 0;

@@ -9,6 +9,7 @@ namespace attn_internal {
 
 namespace {
 std::atomic<uint64_t> g_timeout_ns{kDefaultWaitTimeoutNs};
+std::atomic<int> g_schedule{ATTN_SCHEDULE_PINGPONG};
 std::atomic<int> g_last_cuda_error{0};
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -32,6 +33,7 @@ EncodeTiledFn encode_fn() {
 }  // namespace
 
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
+int schedule_mode() { return g_schedule.load(std::memory_order_relaxed); }
 
 void record_cuda_error(cudaError_t e) {
   if (e != cudaSuccess) g_last_cuda_error.store(static_cast<int>(e));
@@ -86,6 +88,12 @@ ATTN_EXPORT attn_status attn_get_device_status(void* stream) {
 
 ATTN_EXPORT void attn_set_wait_timeout_ns(uint64_t timeout_ns) {
   g_timeout_ns.store(timeout_ns ? timeout_ns : kDefaultWaitTimeoutNs);
+}
+
+ATTN_EXPORT attn_status attn_set_schedule(int mode) {
+  if (mode != ATTN_SCHEDULE_PINGPONG && mode != ATTN_SCHEDULE_ONE_TILE) return ATTN_ERR_INVALID_ARG;
+  g_schedule.store(mode);
+  return ATTN_OK;
 }
 
 ATTN_EXPORT int attn_last_cuda_error(void) { return g_last_cuda_error.load(); }

@@ -27,6 +27,7 @@ enum : unsigned int {
 constexpr uint64_t kDefaultWaitTimeoutNs = 1000000000ull;
 
 uint64_t wait_timeout_ns();
+int schedule_mode();  // ATTN_SCHEDULE_* of later launches
 void record_cuda_error(cudaError_t e);
 attn_status cuda_status(cudaError_t e);  // records and maps to ATTN_OK / ATTN_ERR_CUDA
 

@@ -191,6 +191,21 @@ attn_status attn_get_device_status(void* stream);
 void attn_set_wait_timeout_ns(uint64_t timeout_ns);
 
 /*
+ * attn_set_schedule -- work schedule of later launches with two Q tiles per
+ * CTA (d <= 128), process-wide; an ablation switch in the spirit of the
+ * FlashAttention-3 page's overlap ablation ("Overlapping GEMM and Softmax").
+ *   ATTN_SCHEDULE_PINGPONG (default): each CTA holds two 128-row Q tiles and
+ *       the softmax of one overlaps the matrix products of the other.
+ *   ATTN_SCHEDULE_ONE_TILE: each CTA works on one Q tile at a time (the same
+ *       kernel with the second tile idle), so softmax and products of a tile
+ *       alternate without overlap.  Same results, bit for bit.
+ * Returns ATTN_ERR_INVALID_ARG for any other value (the mode is unchanged).
+ */
+#define ATTN_SCHEDULE_PINGPONG 0
+#define ATTN_SCHEDULE_ONE_TILE 1
+attn_status attn_set_schedule(int mode);
+
+/*
  * attn_debug_bounded_wait -- launches one tiny kernel that waits on a barrier
  * nothing ever signals, using the same bounded wait as the attention kernels,
  * with limit `timeout_ns`.  It exists so that the timeout path can be tested

@@ -22,6 +22,13 @@ def test_every_declared_symbol_is_exported(lib):
     assert not missing, f"declared in include/attn.h but not exported: {missing}"
 
 
+def test_schedule_switch(lib):
+    assert lib.attn_set_schedule(7) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_set_schedule(-1) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_set_schedule(attn.SCHEDULE_ONE_TILE) == attn.ATTN_OK
+    assert lib.attn_set_schedule(attn.SCHEDULE_PINGPONG) == attn.ATTN_OK
+
+
 def test_status_strings_and_version(lib):
     assert attn.status_string(attn.ATTN_OK) == "ATTN_OK"
     assert attn.status_string(attn.ATTN_ERR_TIMEOUT) == "ATTN_ERR_TIMEOUT"

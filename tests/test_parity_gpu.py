@@ -150,6 +150,24 @@ def test_host_pipeline_chunks_match_device_path(B, H, d):
     assert attn.device_status() == attn.ATTN_OK
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_one_tile_schedule_matches_pingpong(d):
+    """The overlap ablation (one Q tile per CTA at a time) does the same
+    arithmetic as the ping-pong schedule: identical O and lse."""
+    q, k, v = (t.cuda() for t in parity.inputs(2, 3, 700, d, "bf16", seed=31))
+    try:
+        for causal in (False, True):
+            o_pp, l_pp = attn.attn_fwd(q, k, v, causal=causal)
+            attn.set_schedule(attn.SCHEDULE_ONE_TILE)
+            o_ot, l_ot = attn.attn_fwd(q, k, v, causal=causal)
+            attn.set_schedule(attn.SCHEDULE_PINGPONG)
+            torch.cuda.synchronize()
+            assert torch.equal(o_pp, o_ot) and torch.equal(l_pp, l_ot), (d, causal)
+    finally:
+        attn.set_schedule(attn.SCHEDULE_PINGPONG)
+    assert attn.device_status() == attn.ATTN_OK
+
+
 def test_repeated_calls_are_deterministic():
     q, k, v = (t.cuda() for t in parity.inputs(2, 8, 1000, 128, "bf16", seed=14))
     o1, l1 = attn.attn_fwd(q, k, v, causal=True)
