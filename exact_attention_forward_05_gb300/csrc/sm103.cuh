@@ -214,47 +214,12 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate, bool f8) {
-  if (f8) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  }
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate, bool f8) {
-  if (f8) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  }
-}
-
-// The same two products with each shared-memory descriptor given as its low
-// word (start address >> 4, in the low 14 bits) and high word: for operand
-// addresses below 2^18 the descriptor of (base + 16 k) is the base descriptor
-// with k added to the low word, so the issuing thread spends one add per
-// operand between products.
+// D[tmem] (+)= A[smem] * B[smem] (mma_ss_w) and D[tmem] (+)= A[tmem] * B[smem]
+// (mma_ts_w), each shared-memory descriptor given as its low word (start
+// address >> 4, in the low 14 bits) and high word: for operand addresses below
+// 2^18 the descriptor of (base + 16 k) is the base descriptor with k added to
+// the low word, so the issuing thread spends one add per operand between
+// products.  `accumulate` = 0 overwrites D.
 __device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
                                          uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
                                          uint32_t accumulate, bool f8) {
@@ -294,7 +259,9 @@ __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint3
   }
 }
 
-// High and low words of the 128-byte-swizzle descriptor of smem_desc_sw128.
+// Shared-memory matrix descriptor, 128-byte swizzle (layout type 2 in bits
+// 61-63), version 1 (bit 46): start address, leading and stride byte offsets in
+// 16-byte units (14 bits each, at bits 0, 16 and 32).  High and low 32-bit words.
 __host__ __device__ constexpr uint32_t desc_sw128_hi(uint32_t sbo_bytes) {
   return ((sbo_bytes & 0x3FFFFu) >> 4) | (1u << 14) | (2u << 29);
 }
@@ -308,16 +275,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
-}
-
-// Shared-memory matrix descriptor, 128-byte swizzle (layout type 2), version 1.
-// Addresses and byte offsets are encoded in 16-byte units (14 bits each).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
-                                                    uint32_t sbo_bytes) {
-  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
-         (static_cast<uint64_t>((lbo_bytes & 0x3FFFFu) >> 4) << 16) |
-         (static_cast<uint64_t>((sbo_bytes & 0x3FFFFu) >> 4) << 32) | (1ull << 46) |
-         (2ull << 61);
 }
 
 // Instruction descriptor, dense, fp32 accumulator.  a_fmt/b_fmt: for kind::f16
