@@ -36,7 +36,7 @@ METRIC = "attention fwd TFLOP/s and % of GB300 dense BF16/FP8 tensor peak vs seq
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 KERNEL_SOURCES = [os.path.join(ROOT, "exact_attention_forward_05_gb300", "csrc", f)
-                  for f in ("attn_kernel.cuh", "sm103.cuh", "attn_fwd.cu")]
+                  for f in ("attn_kernel.cuh", "sm103.cuh", "attn_fwd.cu", "host_common.h", "host_common.cu")]
 PROFILE_JSON = os.path.join(ROOT, "profiles", "attn_fwd_bf16_b2_h16_n8192_d128.json")
 
 WORKLOADS = {}

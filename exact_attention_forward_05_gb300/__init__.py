@@ -24,10 +24,13 @@ from . import build as _build
 __all__ = ["attn_fwd", "attn_fwd_host", "fp8_prepare", "attn_fwd_fp8", "attn_fwd_fp8_pipeline", "host_workspace_bytes", "device_status",
            "set_wait_timeout_ns", "set_schedule", "debug_bounded_wait", "status_string", "library_path",
            "AttnError", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
-           "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "exported_symbols"]
+           "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "exported_symbols",
+           "LAYOUT_BHND", "LAYOUT_BNHD"]
 
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_MISALIGNED, ATTN_ERR_CUDA, \
     ATTN_ERR_TIMEOUT = range(6)
+LAYOUT_BHND, LAYOUT_BNHD = 0, 1  # [B, H, N, d] / [B, N, H, d] for q, k, v and o
+_LAYOUTS = {"bhnd": LAYOUT_BHND, "bnhd": LAYOUT_BNHD}
 ATTN_FP16, ATTN_BF16 = 0, 1
 _DTYPES = {torch.float16: ATTN_FP16, torch.bfloat16: ATTN_BF16}
 
@@ -58,6 +61,8 @@ def _load():
                                      ctypes.c_uint64, ctypes.c_size_t)
             lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp]
             lib.attn_fwd.restype = i32
+            lib.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, i32, vp]
+            lib.attn_fwd_ex.restype = i32
             lib.attn_fwd_host_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
             lib.attn_fwd_host_workspace_bytes.restype = sz
             lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32,
@@ -127,29 +132,39 @@ def _shape_of(q, k, v):
 
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
              scale: float | None = None, out: torch.Tensor | None = None,
-             lse: torch.Tensor | None = None, return_lse: bool = True, stream=None):
-    """Exact attention forward on CUDA tensors [B, H, N, d] (fp16 or bf16).
+             lse: torch.Tensor | None = None, return_lse: bool = True, stream=None,
+             layout: str = "bhnd"):
+    """Exact attention forward on CUDA tensors (fp16 or bf16).
 
-    Returns (O, lse) with O like q and lse float32 [B, H, N] (None when
-    ``return_lse`` is false and no ``lse`` buffer is given).
+    ``layout`` is "bhnd" (q, k, v, o are [B, H, N, d]) or "bnhd" ([B, N, H, d],
+    no transpose needed).  Returns (O, lse) with O like q and lse float32
+    [B, H, N] in either layout (None when ``return_lse`` is false and no
+    ``lse`` buffer is given).
     """
+    if layout not in _LAYOUTS:
+        raise ValueError("layout must be 'bhnd' or 'bnhd'")
     B, H, N, d = _shape_of(q, k, v)
+    if layout == "bnhd":
+        H, N = N, H
     if not (q.is_cuda and k.device == q.device and v.device == q.device):
         raise ValueError("q, k, v must be CUDA tensors on one device")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
         out = torch.empty_like(q)
+    if (out.shape != q.shape or out.dtype != q.dtype or out.device != q.device
+            or not out.is_contiguous()):
+        raise ValueError("out must be a contiguous tensor like q")
     if lse is None and return_lse:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous()
-                            or tuple(lse.shape) != (B, H, N)):
-        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+                            or tuple(lse.shape) != (B, H, N) or lse.device != q.device):
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor on q's device")
     with torch.cuda.device(q.device):
-        st = _load().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                              None if lse is None else lse.data_ptr(), B, H, N, d,
-                              int(bool(causal)), float(scale), _DTYPES[q.dtype],
-                              _stream_handle(stream, q.device))
+        st = _load().attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                 None if lse is None else lse.data_ptr(), B, H, N, d,
+                                 int(bool(causal)), float(scale), _DTYPES[q.dtype], _LAYOUTS[layout],
+                                 _stream_handle(stream, q.device))
     _check(st, "attn_fwd")
     return out, lse
 

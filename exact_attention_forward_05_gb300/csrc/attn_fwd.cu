@@ -15,11 +15,12 @@ namespace {
 
 template <int D, int KIND>
 attn_status launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                   int N, int causal, float scale, cudaStream_t stream) {
+                   int N, int causal, float scale, int layout, cudaStream_t stream) {
   FwdParams prm{};
   prm.o = o;
   prm.lse = lse;
   prm.causal = causal ? 1 : 0;
+  prm.layout = layout;
   return attn_kernel::launch_fwd<D, KIND>(q, k, v, prm, B, H, N, scale, stream);
 }
 
@@ -62,21 +63,28 @@ namespace attn_internal {
 cudaError_t fwd_status_exchange(unsigned int* out) { return attn_kernel::status_exchange(out); }
 }  // namespace attn_internal
 
-ATTN_EXPORT attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                                 int H, int N, int d, int causal, float scale, attn_dtype dtype,
-                                 void* stream) {
+ATTN_EXPORT attn_status attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                    int H, int N, int d, int causal, float scale, attn_dtype dtype,
+                                    int layout, void* stream) {
+  if (layout != ATTN_LAYOUT_BHND && layout != ATTN_LAYOUT_BNHD) return ATTN_ERR_INVALID_ARG;
   attn_status st = check_args(q, k, v, o, lse, B, H, N, d, scale, dtype);
   if (st != ATTN_OK || static_cast<int64_t>(B) * H * N == 0) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool bf = dtype == ATTN_BF16;
   switch (d) {
-    case 64: return bf ? launch<64, KIND_BF16>(q, k, v, o, lse, B, H, N, causal, scale, s)
-                       : launch<64, KIND_F16>(q, k, v, o, lse, B, H, N, causal, scale, s);
-    case 128: return bf ? launch<128, KIND_BF16>(q, k, v, o, lse, B, H, N, causal, scale, s)
-                        : launch<128, KIND_F16>(q, k, v, o, lse, B, H, N, causal, scale, s);
-    default: return bf ? launch<256, KIND_BF16>(q, k, v, o, lse, B, H, N, causal, scale, s)
-                       : launch<256, KIND_F16>(q, k, v, o, lse, B, H, N, causal, scale, s);
+    case 64: return bf ? launch<64, KIND_BF16>(q, k, v, o, lse, B, H, N, causal, scale, layout, s)
+                       : launch<64, KIND_F16>(q, k, v, o, lse, B, H, N, causal, scale, layout, s);
+    case 128: return bf ? launch<128, KIND_BF16>(q, k, v, o, lse, B, H, N, causal, scale, layout, s)
+                        : launch<128, KIND_F16>(q, k, v, o, lse, B, H, N, causal, scale, layout, s);
+    default: return bf ? launch<256, KIND_BF16>(q, k, v, o, lse, B, H, N, causal, scale, layout, s)
+                       : launch<256, KIND_F16>(q, k, v, o, lse, B, H, N, causal, scale, layout, s);
   }
+}
+
+ATTN_EXPORT attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                 int H, int N, int d, int causal, float scale, attn_dtype dtype,
+                                 void* stream) {
+  return attn_fwd_ex(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, ATTN_LAYOUT_BHND, stream);
 }
 
 namespace {

@@ -138,6 +138,8 @@ struct FwdParams {
   void* o;
   float* lse;
   int BH, N;
+  int H;       // heads: unit head index bh = b * H + h
+  int layout;  // ATTN_LAYOUT_BHND or ATTN_LAYOUT_BNHD, of q, k, v and o
   int causal;
   float sl2;  // scale * log2(e)
   int units_per_head;
@@ -155,6 +157,19 @@ struct Unit {
   int bh, m0, nkb;
   int nb[2];  // key blocks visited by each Q tile (0 = tile inactive)
 };
+
+// Tensor maps are 4-D over the operand as it lies in memory: [B, H, N, d] as
+// {d, N, H, B}, [B, N, H, d] as {d, H, N, B}.  A tile is 128 rows of one head
+// either way and lands in shared memory the same way; only the order of the
+// row and head coordinates differs.
+__device__ __forceinline__ void tma_load_rows(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
+                                              int row, int b, int h, bool bnhd) {
+  tma_load_4d(dst, map, bar, x, bnhd ? h : row, bnhd ? row : h, b);
+}
+__device__ __forceinline__ void tma_store_rows(const CUtensorMap* map, uint32_t src, int x, int row, int b,
+                                               int h, bool bnhd) {
+  tma_store_4d(map, src, x, bnhd ? h : row, bnhd ? row : h, b);
+}
 
 // Unit order: causal units longest-first (highest query block first, all heads
 // of one query block together); full attention head-major so that CTAs that
@@ -286,7 +301,8 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
       const WaitCtx wc{abort_flag, &g_status_word, p.timeout_ns};
       uint32_t kv_fill = 0, q_iter = 0;
       bool ok = true;
-      auto load_block = [&](const CUtensorMap* map, int j, int bh) -> bool {
+      const bool bnhd = p.layout == ATTN_LAYOUT_BNHD;
+      auto load_block = [&](const CUtensorMap* map, int j, int ub, int uh) -> bool {
         const uint32_t s = kv_fill % C::STAGES;
         const uint32_t ph = (kv_fill / C::STAGES) & 1u;
         if (!mbar_wait(BAR(C::B_KV_EMPTY + s), ph ^ 1u, wc, attn_internal::kStatusTimeoutLoad))
@@ -294,14 +310,14 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         mbar_arrive_expect_tx(BAR(C::B_KV_FULL + s), C::TILE_BYTES);
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c)
-          tma_load_3d(sKV + s * C::TILE_BYTES + c * C::CHUNK_BYTES, map, BAR(C::B_KV_FULL + s),
-                      c * C::CHUNK_ELEMS, j * kBN, bh);
+          tma_load_rows(sKV + s * C::TILE_BYTES + c * C::CHUNK_BYTES, map, BAR(C::B_KV_FULL + s),
+                        c * C::CHUNK_ELEMS, j * kBN, ub, uh, bnhd);
         ++kv_fill;
         return true;
       };
       // Pair slot s holds K_j in tile 2s and V_{j-1} in tile 2s+1 (either may
       // be absent at the ends of a unit: step 0 has no V, step nbmax no K).
-      auto load_pair = [&](int j, int nbmax, int bh) -> bool {
+      auto load_pair = [&](int j, int nbmax, int ub, int uh) -> bool {
         const uint32_t s = kv_fill % C::RING;
         const uint32_t ph = (kv_fill / C::RING) & 1u;
         if (!mbar_wait(BAR(C::B_KV_EMPTY + s), ph ^ 1u, wc, attn_internal::kStatusTimeoutLoad))
@@ -311,11 +327,11 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c) {
           if (has_k)
-            tma_load_3d(sKV + (2 * s) * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmK,
-                        BAR(C::B_KV_FULL + s), c * C::CHUNK_ELEMS, j * kBN, bh);
+            tma_load_rows(sKV + (2 * s) * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmK,
+                          BAR(C::B_KV_FULL + s), c * C::CHUNK_ELEMS, j * kBN, ub, uh, bnhd);
           if (has_v)
-            tma_load_3d(sKV + (2 * s + 1) * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmV,
-                        BAR(C::B_KV_FULL + s), c * C::CHUNK_ELEMS, (j - 1) * kBN, bh);
+            tma_load_rows(sKV + (2 * s + 1) * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmV,
+                          BAR(C::B_KV_FULL + s), c * C::CHUNK_ELEMS, (j - 1) * kBN, ub, uh, bnhd);
         }
         ++kv_fill;
         return true;
@@ -327,6 +343,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         const Unit w = decode_unit<NQ>(u, p);
         const int nbmax = max(w.nb[0], w.nb[1]);
         if (nbmax == 0) continue;  // no query row of this entry is below N
+        const int ub = w.bh / p.H, uh = w.bh - ub * p.H;
         if (!mbar_wait(BAR(C::B_Q_EMPTY), (q_iter & 1u) ^ 1u, wc, attn_internal::kStatusTimeoutLoad)) {
           ok = false;
           break;
@@ -338,16 +355,16 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
           if (w.nb[t] == 0) continue;
 #pragma unroll
           for (int c = 0; c < C::CHUNKS; ++c)
-            tma_load_3d(sQ + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmQ, BAR(C::B_Q_FULL),
-                        c * C::CHUNK_ELEMS, w.m0 + kBM * t, w.bh);
+            tma_load_rows(sQ + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tmQ, BAR(C::B_Q_FULL),
+                          c * C::CHUNK_ELEMS, w.m0 + kBM * t, ub, uh, bnhd);
         }
         // K/V in the order the MMA warp consumes them: K_0, then (K_j, V_{j-1}).
         for (int j = 0; j <= nbmax && ok; ++j) {
           if constexpr (C::KV_PAIRS) {
-            ok = load_pair(j, nbmax, w.bh);
+            ok = load_pair(j, nbmax, ub, uh);
           } else {
-            if (j < nbmax) ok = load_block(&tmK, j, w.bh);
-            if (ok && j >= 1) ok = load_block(&tmV, j - 1, w.bh);
+            if (j < nbmax) ok = load_block(&tmK, j, ub, uh);
+            if (ok && j >= 1) ok = load_block(&tmV, j - 1, ub, uh);
           }
         }
       }
@@ -685,6 +702,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
       const uint32_t ost = smem_u32(smem + C::OFF_OST + wg * C::OST_BYTES);
       const uint32_t ost_row = ost + static_cast<uint32_t>(row) * 128u;
       const uint32_t swz = static_cast<uint32_t>(row & 7);
+      const int ob = w.bh / p.H, oh = w.bh - ob * p.H;
 #pragma unroll 1
       for (int c2 = 0; c2 < D / 64; ++c2) {
         uint32_t o[2][32];
@@ -711,7 +729,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         fence_proxy_async_smem();
         bar_sync_n(tile_bar, 128);
         if (wq == 0 && lane == 0) {
-          tma_store_3d(&tmO, ost, 64 * c2, tile_row0, w.bh);
+          tma_store_rows(&tmO, ost, 64 * c2, tile_row0, ob, oh, p.layout == ATTN_LAYOUT_BNHD);
           bulk_commit_group();
         }
       }
@@ -744,10 +762,19 @@ attn_status launch_fwd(const void* q, const void* k, const void* v, FwdParams pr
   const uint64_t BH = static_cast<uint64_t>(B) * H;
   CUtensorMap mq, mk, mv, mo;
   const CUtensorMapDataType dto = KIND == KIND_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (!attn_internal::encode_tmap_3d(&mq, dt, q, D, N, BH, C::ELEM, C::CHUNK_ELEMS, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !attn_internal::encode_tmap_3d(&mk, dt, k, D, N, BH, C::ELEM, C::CHUNK_ELEMS, kBN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !attn_internal::encode_tmap_3d(&mv, dt, v, D, N, BH, C::ELEM, C::CHUNK_ELEMS, kBN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !attn_internal::encode_tmap_3d(&mo, dto, prm.o, D, N, BH, 2, 64, kBM, CU_TENSOR_MAP_SWIZZLE_128B))
+  // {d, N, H, B} for [B, H, N, d], {d, H, N, B} for [B, N, H, d]; the box is
+  // box_x elements of `rows` consecutive rows of one head.
+  const bool bnhd = prm.layout == ATTN_LAYOUT_BNHD;
+  auto encode = [&](CUtensorMap* m, CUtensorMapDataType t, const void* base, uint64_t elem, uint32_t box_x,
+                    uint32_t rows) {
+    const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(bnhd ? H : N),
+                              static_cast<uint64_t>(bnhd ? N : H), static_cast<uint64_t>(B)};
+    const uint64_t strides[3] = {D * elem, dims[1] * D * elem, dims[2] * dims[1] * D * elem};
+    const uint32_t box[4] = {box_x, bnhd ? 1u : rows, bnhd ? rows : 1u, 1u};
+    return attn_internal::encode_tmap_4d(m, t, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  };
+  if (!encode(&mq, dt, q, C::ELEM, C::CHUNK_ELEMS, kBM) || !encode(&mk, dt, k, C::ELEM, C::CHUNK_ELEMS, kBN) ||
+      !encode(&mv, dt, v, C::ELEM, C::CHUNK_ELEMS, kBN) || !encode(&mo, dto, prm.o, 2, 64, kBM))
     return ATTN_ERR_CUDA;
 
   static int configured_for[64] = {0};  // per device: dynamic shared memory attribute set
@@ -761,6 +788,7 @@ attn_status launch_fwd(const void* q, const void* k, const void* v, FwdParams pr
     if (dev < 64) configured_for[dev] = 1;
   }
   prm.BH = static_cast<int>(BH);
+  prm.H = H;
   prm.N = N;
   prm.sl2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.units_per_head = (N + kBM * C::NQ - 1) / (kBM * C::NQ);

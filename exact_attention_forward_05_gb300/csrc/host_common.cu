@@ -58,16 +58,16 @@ int sm_count() {
   return n;
 }
 
-bool encode_tmap_3d(CUtensorMap* out, CUtensorMapDataType dtype, const void* base, uint64_t inner,
-                    uint64_t rows, uint64_t outer, uint32_t elem_bytes, uint32_t box_inner,
-                    uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+bool encode_tmap_4d(CUtensorMap* out, CUtensorMapDataType dtype, const void* base,
+                    const uint64_t (&dims)[4], const uint64_t (&strides)[3], const uint32_t (&box)[4],
+                    CUtensorMapSwizzle swizzle) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[3] = {inner, rows, outer};
-  const cuuint64_t strides[2] = {inner * elem_bytes, inner * rows * elem_bytes};
-  const cuuint32_t box[3] = {box_inner, box_rows, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(out, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
+  const cuuint64_t gdims[4] = {dims[0], dims[1], dims[2], dims[3]};
+  const cuuint64_t gstrides[3] = {strides[0], strides[1], strides[2]};
+  const cuuint32_t gbox[4] = {box[0], box[1], box[2], box[3]};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(out, dtype, 4, const_cast<void*>(base), gdims, gstrides, gbox, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;

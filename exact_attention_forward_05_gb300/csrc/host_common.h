@@ -34,12 +34,12 @@ attn_status cuda_status(cudaError_t e);  // records and maps to ATTN_OK / ATTN_E
 // Multiprocessor count of the current device (cached per device).
 int sm_count();
 
-// Encode a 3-D tiled TMA descriptor over a contiguous [outer, rows, inner]
-// tensor with element size `elem_bytes`; box = {box_inner, box_rows, 1}.
-// Out-of-bounds elements of a load read as zero.  Returns false on failure.
-bool encode_tmap_3d(CUtensorMap* out, CUtensorMapDataType dtype, const void* base, uint64_t inner,
-                    uint64_t rows, uint64_t outer, uint32_t elem_bytes, uint32_t box_inner,
-                    uint32_t box_rows, CUtensorMapSwizzle swizzle);
+// Encode a 4-D tiled TMA descriptor: dims[0] is contiguous, strides[i] is the
+// byte stride of dims[i + 1] (a multiple of 16).  Out-of-bounds elements of a
+// load read as zero; a store skips them.  Returns false on failure.
+bool encode_tmap_4d(CUtensorMap* out, CUtensorMapDataType dtype, const void* base,
+                    const uint64_t (&dims)[4], const uint64_t (&strides)[3], const uint32_t (&box)[4],
+                    CUtensorMapSwizzle swizzle);
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 

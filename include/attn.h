@@ -19,6 +19,7 @@
  * Conventions shared by every entry point:
  *  - Layout: Q, K, V, O are contiguous [B, H, N, d] (row-major, d innermost);
  *    self-attention, so queries and keys share N.  lse is contiguous [B, H, N].
+ *    attn_fwd_ex also takes Q, K, V, O as contiguous [B, N, H, d].
  *  - Device pointers are CUDA device addresses on the current device; every
  *    tensor base must be 16-byte aligned (lse: 4-byte aligned).
  *  - Ownership: the caller owns every buffer.  The library never allocates
@@ -54,6 +55,10 @@ typedef enum {
 
 typedef enum { ATTN_FP16 = 0, ATTN_BF16 = 1 } attn_dtype;
 
+/* Memory layout of Q, K, V and O (lse is [B, H, N] in both). */
+#define ATTN_LAYOUT_BHND 0 /* [B, H, N, d]: each head's rows contiguous */
+#define ATTN_LAYOUT_BNHD 1 /* [B, N, H, d]: each token's heads contiguous */
+
 /*
  * attn_fwd -- exact attention forward, 16-bit inputs and output.
  *
@@ -72,6 +77,18 @@ typedef enum { ATTN_FP16 = 0, ATTN_BF16 = 1 } attn_dtype;
  */
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                      int N, int d, int causal, float scale, attn_dtype dtype, void* stream);
+
+/*
+ * attn_fwd_ex -- attn_fwd with the memory layout of Q, K, V and O chosen by
+ * `layout`: ATTN_LAYOUT_BHND ([B, H, N, d], exactly attn_fwd) or
+ * ATTN_LAYOUT_BNHD ([B, N, H, d], the layout a projection of [B, N, H*d]
+ * activations gives, so that no transpose is needed).  lse is [B, H, N] either
+ * way.  The results are the same values, element for element, as attn_fwd on
+ * the inputs transposed to [B, H, N, d].  Any other `layout` returns
+ * ATTN_ERR_INVALID_ARG; the other arguments, rules and errors are attn_fwd's.
+ */
+attn_status attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                        int N, int d, int causal, float scale, attn_dtype dtype, int layout, void* stream);
 
 /*
  * attn_fwd_host_workspace_bytes -- device workspace (bytes) attn_fwd_host needs

@@ -58,6 +58,31 @@ def test_validation_before_launch(lib):
     assert _fwd(lib, B=65536, H=65536) == attn.ATTN_ERR_INVALID_ARG
 
 
+def test_layout_argument(lib):
+    def fwd_ex(layout, **kw):
+        a = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, B=1, H=1, N=8, d=128)
+        a.update(kw)
+        return lib.attn_fwd_ex(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["d"],
+                               0, 0.1, attn.ATTN_BF16, layout, None)
+    assert attn.LAYOUT_BHND == 0 and attn.LAYOUT_BNHD == 1
+    for bad in (2, -1, 7):
+        assert fwd_ex(bad) == attn.ATTN_ERR_INVALID_ARG
+    # The layout check comes first; the remaining checks are attn_fwd's.
+    assert fwd_ex(2, N=0) == attn.ATTN_ERR_INVALID_ARG
+    assert fwd_ex(attn.LAYOUT_BNHD, d=96) == attn.ATTN_ERR_UNSUPPORTED
+    assert fwd_ex(attn.LAYOUT_BNHD, q=0x1008) == attn.ATTN_ERR_MISALIGNED
+    assert fwd_ex(attn.LAYOUT_BNHD, N=0, q=None, k=None, v=None, o=None) == attn.ATTN_OK
+
+
+def test_python_layout_and_out_checks(lib):
+    import torch
+    q = torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        attn.attn_fwd(q, q, q, layout="nhd")
+    with pytest.raises(ValueError):  # host tensors
+        attn.attn_fwd(q, q, q, layout="bnhd")
+
+
 def test_empty_problem_launches_nothing(lib):
     # B*H*N == 0 is a valid no-op: ATTN_OK without touching CUDA or the pointers.
     assert _fwd(lib, N=0, q=None, k=None, v=None, o=None) == attn.ATTN_OK

@@ -174,3 +174,39 @@ def test_repeated_calls_are_deterministic():
     o2, l2 = attn.attn_fwd(q, k, v, causal=True)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("N", [129, 300])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_bnhd_layout(d, N, dtype):
+    """q, k, v, o as [B, N, H, d]: every row against the oracle, and the same
+    bits as the [B, H, N, d] launch on the transposed inputs.  The output sits
+    in a buffer one batch longer, filled with NaN: rows past N must stay
+    unwritten."""
+    B, H = 2, 3
+    q, k, v = parity.inputs(B, H, N, d, dtype, seed=41 + d + N)
+    qt, kt, vt = (t.transpose(1, 2).contiguous().cuda() for t in (q, k, v))
+    for causal in (False, True):
+        big = torch.full((B + 1, N, H, d), float("nan"), dtype=qt.dtype, device="cuda")
+        o, lse = attn.attn_fwd(qt, kt, vt, causal=causal, out=big[:B], layout="bnhd")
+        o_ref, lse_ref = attn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal)
+        torch.cuda.synchronize()
+        assert torch.isnan(big[B]).all(), "rows past the end written"
+        assert torch.equal(o.transpose(1, 2), o_ref) and torch.equal(lse, lse_ref), (d, N, causal)
+        m = parity.metrics(o.transpose(1, 2), lse, *oracle.attention(q, k, v, causal=causal, scale=d ** -0.5))
+        parity.assert_close(m, what=f"bnhd d={d} N={N} {dtype} causal={causal}")
+    assert attn.device_status() == attn.ATTN_OK
+
+
+def test_bnhd_layout_many_units():
+    """[B, N, H, d] over several persistent rounds (B=2, H=16, N=2048, d=128):
+    the same bits as the [B, H, N, d] launch."""
+    q, k, v = (t.cuda() for t in parity.inputs(2, 16, 2048, 128, "bf16", seed=43))
+    qt, kt, vt = (t.transpose(1, 2).contiguous() for t in (q, k, v))
+    for causal in (False, True):
+        o, lse = attn.attn_fwd(qt, kt, vt, causal=causal, layout="bnhd")
+        o_ref, lse_ref = attn.attn_fwd(q, k, v, causal=causal)
+        torch.cuda.synchronize()
+        assert torch.equal(o.transpose(1, 2), o_ref) and torch.equal(lse, lse_ref), causal
+    assert attn.device_status() == attn.ATTN_OK
