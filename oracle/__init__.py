@@ -8,7 +8,9 @@ Definitions (each cited where it is computed, in ``oracle.c``):
 
 * ``attention``: softmax(scale * Q K^T [+ causal mask]) V and the per-row
   logsumexp, exactly as the "Standard Attention" section of "FlashAttention --
-  one, two, three!" lays it out (three plain passes, N x N scores per head).
+  one, two, three!" lays it out (three plain passes, Nq x Nk scores per head;
+  for Nq != Nk the causal mask is aligned at the first positions, causal=1 or
+  True, or at the last positions, causal=2).
 * ``e4m3_encode`` / ``e4m3_decode``: OCP E4M3 codec, round to nearest even,
   saturating at +-448.
 * ``hadamard_rotate``: x -> (x * sigma) H_d / sqrt(d) with the Sylvester
@@ -65,6 +67,9 @@ def _load():
             lib.oracle_attention.argtypes = [dp, dp, dp, dp, dp, i64, i64, i64, i32,
                                              ctypes.c_double, dp, i64, i32, dp]
             lib.oracle_attention.restype = i32
+            lib.oracle_attention_qk.argtypes = [dp, dp, dp, dp, dp, i64, i64, i64, i64, i32,
+                                                ctypes.c_double, dp, i64, i32, dp]
+            lib.oracle_attention_qk.restype = i32
             lib.oracle_e4m3_decode.argtypes = [dp, dp, i64]
             lib.oracle_e4m3_encode.argtypes = [dp, dp, i64]
             lib.oracle_hadamard_entry.argtypes = [i64, i64]
@@ -91,13 +96,19 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, rows=No
               nthreads: int = 0, return_threads: bool = False):
     """Exact attention in float64.
 
-    q, k, v: [B, H, N, d] (torch CPU tensors or numpy arrays, any float dtype;
-    values are widened exactly).  ``rows``: optional sorted query-row subset,
-    applied to every head.  Returns (O [B, H, R, d], lse [B, H, R]) float64,
-    plus the thread count when ``return_threads``.
+    q: [B, H, Nq, d], k, v: [B, H, Nk, d] (torch CPU tensors or numpy arrays,
+    any float dtype; values are widened exactly).  ``causal``: False / 0 (no
+    mask), True / 1 (query i sees keys j <= i), 2 (query i sees keys
+    j <= i + Nk - Nq).  ``rows``: optional sorted query-row subset, applied to
+    every head.  Returns (O [B, H, R, d], lse [B, H, R]) float64, plus the
+    thread count when ``return_threads``.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, N, d = q.shape
+    if k.shape != v.shape or k.shape[:2] != (B, H) or k.shape[3] != d:
+        raise ValueError("k, v must be [B, H, Nk, d] with q's B, H and d")
+    Nk = k.shape[2]
+    mode = int(causal)
     if scale is None:
         scale = 1.0 / np.sqrt(d)
     rows_arr = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
@@ -105,8 +116,8 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, rows=No
     o = np.empty((B, H, R, d), dtype=np.float64)
     lse = np.empty((B, H, R), dtype=np.float64)
     used = ctypes.c_int(0)
-    st = _load().oracle_attention(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B * H, N, d, int(bool(causal)),
+    st = _load().oracle_attention_qk(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B * H, N, Nk, d, mode,
         float(scale), None if rows_arr is None else _ptr(rows_arr), R, int(nthreads),
         ctypes.cast(ctypes.pointer(used), ctypes.c_void_p))
     if st != 0:

@@ -9,11 +9,18 @@
  * say the fused kernels reproduce exactly ("FlashAttention -- one, two,
  * three!", section "Standard Attention"; comrad404 review, "Коротко" and FAQ):
  *
- *   s_ij  = scale * sum_c q_ic k_jc          for keys j < N (causal: j <= i)
+ *   s_ij  = scale * sum_c q_ic k_jc          for the visible keys j of row i
  *   m_i   = max_j s_ij
  *   l_i   = sum_j exp(s_ij - m_i)
  *   o_ic  = sum_j exp(s_ij - m_i) v_jc / l_i
  *   lse_i = m_i + ln l_i
+ *
+ * Queries i < Nq, keys j < Nk.  Visible keys: every j (no mask); j <= i
+ * (causal mode 1, queries and keys aligned at their first positions, which is
+ * the causal mask of self-attention when Nq = Nk); j <= i + Nk - Nq (causal
+ * mode 2, aligned at their last positions: the queries are the last Nq of the
+ * Nk positions).  The pages define the causal mask for self-attention only;
+ * both modes are the readings this library takes for Nq != Nk.
  *
  * Each query row is independent, so rows are spread over POSIX threads; every
  * row is computed whole (no blocking, no online softmax).
@@ -39,9 +46,9 @@
 typedef struct {
     const double *q, *k, *v;
     double *o, *lse;
-    int64_t BH, N, d, R;        /* R = number of rows computed per head */
-    const int64_t *rows;         /* NULL: rows 0..N-1 */
-    int causal;
+    int64_t BH, Nq, Nk, d, R;   /* R = number of rows computed per head */
+    const int64_t *rows;         /* NULL: rows 0..Nq-1 */
+    int causal;                  /* 0 none, 1 aligned at the start, 2 at the end */
     double scale;
     int tid, nthreads;
     int status;
@@ -49,16 +56,18 @@ typedef struct {
 
 static void *att_worker(void *arg) {
     att_job *J = (att_job *)arg;
-    double *w = (double *)malloc(sizeof(double) * (size_t)J->N);
+    double *w = (double *)malloc(sizeof(double) * (size_t)(J->Nk > 0 ? J->Nk : 1));
     if (!w) { J->status = 1; return NULL; }
     const int64_t total = J->BH * J->R;
     for (int64_t item = J->tid; item < total; item += J->nthreads) {
         const int64_t bh = item / J->R, r = item % J->R;
         const int64_t i = J->rows ? J->rows[r] : r;          /* query row index */
-        const double *qi = J->q + (bh * J->N + i) * J->d;
-        const double *kh = J->k + bh * J->N * J->d;
-        const double *vh = J->v + bh * J->N * J->d;
-        const int64_t nkeys = J->causal ? i + 1 : J->N;      /* keys 0..nkeys-1 */
+        const double *qi = J->q + (bh * J->Nq + i) * J->d;
+        const double *kh = J->k + bh * J->Nk * J->d;
+        const double *vh = J->v + bh * J->Nk * J->d;
+        int64_t nkeys = J->Nk;                               /* keys 0..nkeys-1 */
+        if (J->causal == 1 && i + 1 < nkeys) nkeys = i + 1;
+        if (J->causal == 2) nkeys = i + 1 + (J->Nk - J->Nq);
         double m = -INFINITY;
         for (int64_t j = 0; j < nkeys; ++j) {
             double dot = 0.0;
@@ -82,18 +91,22 @@ static void *att_worker(void *arg) {
     return NULL;
 }
 
-/* q, k, v: [BH, N, d] float64.  o: [BH, R, d], lse: [BH, R] (may be NULL),
- * where R = nrows if rows != NULL (row indices in [0, N)), else N.
- * nthreads <= 0 uses every online core.  Returns 0 on success; writes the
+/* q: [BH, Nq, d], k, v: [BH, Nk, d] float64.  o: [BH, R, d], lse: [BH, R]
+ * (may be NULL), where R = nrows if rows != NULL (row indices in [0, Nq)),
+ * else Nq.  causal: 0, 1 or 2 as above; a row with no visible key (Nk = 0, or
+ * mode 2 with Nq > Nk) has no softmax and is rejected.  nthreads <= 0 uses
+ * every online core.  Returns 0 on success (2: bad arguments); writes the
  * number of threads used to *threads_used (may be NULL). */
-ORACLE_API int oracle_attention(const double *q, const double *k, const double *v,
-                                double *o, double *lse, int64_t BH, int64_t N, int64_t d,
-                                int causal, double scale, const int64_t *rows, int64_t nrows,
-                                int nthreads, int *threads_used) {
-    if (!q || !k || !v || !o || BH < 0 || N < 0 || d < 1) return 2;
-    const int64_t R = rows ? nrows : N;
+ORACLE_API int oracle_attention_qk(const double *q, const double *k, const double *v,
+                                   double *o, double *lse, int64_t BH, int64_t Nq, int64_t Nk,
+                                   int64_t d, int causal, double scale, const int64_t *rows,
+                                   int64_t nrows, int nthreads, int *threads_used) {
+    if (!q || !k || !v || !o || BH < 0 || Nq < 0 || Nk < 0 || d < 1) return 2;
+    if (causal < 0 || causal > 2) return 2;
+    if (Nq > 0 && (Nk == 0 || (causal == 2 && Nq > Nk))) return 2;
+    const int64_t R = rows ? nrows : Nq;
     for (int64_t r = 0; rows && r < nrows; ++r)
-        if (rows[r] < 0 || rows[r] >= N) return 2;
+        if (rows[r] < 0 || rows[r] >= Nq) return 2;
     if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
     if (nthreads < 1) nthreads = 1;
     if (BH * R < nthreads) nthreads = (int)(BH * R > 0 ? BH * R : 1);
@@ -102,7 +115,7 @@ ORACLE_API int oracle_attention(const double *q, const double *k, const double *
     pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
     if (!jobs || !th) { free(jobs); free(th); return 1; }
     for (int t = 0; t < nthreads; ++t) {
-        att_job J = {q, k, v, o, lse, BH, N, d, R, rows, causal, scale, t, nthreads, 0};
+        att_job J = {q, k, v, o, lse, BH, Nq, Nk, d, R, rows, causal, scale, t, nthreads, 0};
         jobs[t] = J;
     }
     int st = 0;
@@ -115,6 +128,15 @@ ORACLE_API int oracle_attention(const double *q, const double *k, const double *
     free(jobs);
     free(th);
     return st;
+}
+
+/* Self-attention (Nq = Nk = N); causal: 0 none, nonzero the causal mask. */
+ORACLE_API int oracle_attention(const double *q, const double *k, const double *v,
+                                double *o, double *lse, int64_t BH, int64_t N, int64_t d,
+                                int causal, double scale, const int64_t *rows, int64_t nrows,
+                                int nthreads, int *threads_used) {
+    return oracle_attention_qk(q, k, v, o, lse, BH, N, N, d, causal ? 1 : 0, scale, rows, nrows,
+                               nthreads, threads_used);
 }
 
 /* ------------------------------------------------------------ E4M3 codec */

@@ -14,19 +14,20 @@ from tests import pins  # noqa: E402
 def main(lib_path):
     lib = ctypes.CDLL(lib_path)
     i64, dp, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
-    fn = lib.oracle_attention
-    fn.argtypes = [dp, dp, dp, dp, dp, i64, i64, i64, i32, ctypes.c_double, dp, i64, i32, dp]
+    fn = lib.oracle_attention_qk
+    fn.argtypes = [dp, dp, dp, dp, dp, i64, i64, i64, i64, i32, ctypes.c_double, dp, i64, i32, dp]
     fn.restype = i32
 
     def attn(q, k, v, causal, scale, rows=None):
         q, k, v = (np.ascontiguousarray(a, dtype=np.float64) for a in (q, k, v))
         B, H, N, d = q.shape
+        Nk = k.shape[2]
         r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
         R = N if r is None else len(r)
         o = np.empty((B, H, R, d))
         lse = np.empty((B, H, R))
         p = lambda a: ctypes.c_void_p(a.ctypes.data)
-        st = fn(p(q), p(k), p(v), p(o), p(lse), B * H, N, d, int(causal), float(scale),
+        st = fn(p(q), p(k), p(v), p(o), p(lse), B * H, N, Nk, d, int(causal), float(scale),
                 None if r is None else p(r), R, 2, None)
         assert st == 0
         return o, lse

@@ -1,7 +1,8 @@
 """Checks that pin the float64 attention oracle to facts other than its own code.
 
 Every check takes ``attn(q, k, v, causal, scale, rows=None) -> (O, lse)`` on
-float64 [B, H, N, d] arrays, so the same checks run against the real oracle
+float64 arrays, q [B, H, Nq, d] and k, v [B, H, Nk, d] (causal: 0 / False no
+mask, 1 / True keys j <= i, 2 keys j <= i + Nk - Nq), so the same checks run against the real oracle
 (tests/test_oracle_pins.py) and against deliberately broken copies of it
 (tests/test_oracle_mutants.py), which must each fail at least one check.
 
@@ -13,6 +14,9 @@ Sources of truth (none of them is the oracle's formula retyped):
   through V = identity), joint permutation of keys and values, a per-row logit
   shift, an orthogonal change of basis shared by Q and K;
 * a brute-force row-by-row evaluation in pure Python without max subtraction;
+* for Nq != Nk: the same closed forms with the visible-key counts of each mask,
+  and the end-aligned mask as the last rows of self-attention over a longer
+  query sequence;
 * hand-worked examples stored in tests/golden/two_key_softmax.json.
 """
 from __future__ import annotations
@@ -139,16 +143,26 @@ def check_orthogonal_invariance(attn):
         np.testing.assert_allclose(l2, l1, rtol=0, atol=1e-11)
 
 
+def visible_keys(i, Nq, Nk, causal):
+    """Number of keys query row i sees (keys 0 .. count-1)."""
+    if int(causal) == 1:
+        return min(i + 1, Nk)
+    if int(causal) == 2:
+        return i + 1 + (Nk - Nq)
+    return Nk
+
+
 def brute_force(q, k, v, causal, scale):
     """Row by row in pure Python: weights exp(s) with no max subtraction
     (inputs keep |s| small), normalised by their plain sum."""
     B, H, N, d = q.shape
+    Nk = k.shape[2]
     o = np.zeros((B, H, N, d))
     lse = np.zeros((B, H, N))
     for b in range(B):
         for h in range(H):
             for i in range(N):
-                keys = range(i + 1) if causal else range(N)
+                keys = range(visible_keys(i, N, Nk, causal))
                 weights = []
                 for j in keys:
                     s = scale * sum(float(q[b, h, i, c]) * float(k[b, h, j, c]) for c in range(d))
@@ -171,6 +185,55 @@ def check_brute_force(attn):
             ob, lb = brute_force(q, k, v, causal, scale)
             np.testing.assert_allclose(o, ob, rtol=0, atol=1e-12)
             np.testing.assert_allclose(lse, lb, rtol=0, atol=1e-12)
+
+
+def check_brute_force_cross(attn):
+    """Nq != Nk (and the end-aligned mask at Nq = Nk) against the pure-Python
+    evaluation."""
+    for (B, H, Nq, Nk, d), seed in (((1, 2, 5, 9, 3), 34), ((2, 1, 9, 5, 4), 35),
+                                    ((1, 1, 1, 7, 2), 36), ((1, 1, 6, 6, 3), 37)):
+        q = _rand((B, H, Nq, d), seed)
+        k, v = _rand((B, H, Nk, d), seed + 100), _rand((B, H, Nk, d), seed + 200)
+        scale = 0.8 / math.sqrt(d)
+        for causal in (0, 1, 2):
+            if causal == 2 and Nq > Nk:
+                continue
+            o, lse = attn(q, k, v, causal, scale)
+            ob, lb = brute_force(q, k, v, causal, scale)
+            np.testing.assert_allclose(o, ob, rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse, lb, rtol=0, atol=1e-12)
+
+
+def check_cross_zero_query(attn):
+    """Q = 0 with Nq != Nk: O_i is the mean of the V rows row i sees and lse_i
+    the log of their count, for each mask (counts counted here by hand: all Nk;
+    min(i+1, Nk) from the start; i+1+Nk-Nq from the end)."""
+    B, H, d = 2, 2, 4
+    for Nq, Nk in ((13, 29), (29, 13), (1, 5)):
+        q = np.zeros((B, H, Nq, d))
+        k, v = _rand((B, H, Nk, d), 50 + Nq), _rand((B, H, Nk, d), 60 + Nq)
+        for causal in (0, 1, 2):
+            if causal == 2 and Nq > Nk:
+                continue
+            o, lse = attn(q, k, v, causal, 0.6)
+            for i in range(Nq):
+                n = {0: Nk, 1: min(i + 1, Nk), 2: i + 1 + Nk - Nq}[causal]
+                np.testing.assert_allclose(o[:, :, i], v[:, :, :n].mean(axis=2), rtol=0, atol=1e-12)
+                np.testing.assert_allclose(lse[:, :, i], math.log(n), rtol=0, atol=1e-12)
+
+
+def check_end_aligned_is_suffix_of_self_attention(attn):
+    """Causal mask aligned at the end: the Nq queries are the last Nq positions
+    of an Nk-long sequence, so their rows equal the last Nq rows of causal
+    self-attention of [X; Q] over the same keys, whatever X is."""
+    B, H, Nq, Nk, d = 1, 2, 7, 20, 5
+    q = _rand((B, H, Nq, d), 70)
+    x = _rand((B, H, Nk - Nq, d), 71, 4.0)
+    k, v = _rand((B, H, Nk, d), 72), _rand((B, H, Nk, d), 73)
+    o, lse = attn(q, k, v, 2, 0.5)
+    o_self, lse_self = attn(np.concatenate([x, q], axis=2), k, v, 1, 0.5)
+    np.testing.assert_allclose(o, o_self[:, :, Nk - Nq:], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_self[:, :, Nk - Nq:], rtol=0, atol=1e-12)
 
 
 def check_golden(attn):
@@ -204,4 +267,5 @@ def check_row_subset(attn):
 ALL_CHECKS = [check_zero_query_is_mean, check_zero_scale_is_mean, check_causal_row0,
               check_constant_v, check_weights_are_probabilities, check_key_permutation,
               check_logit_shift, check_orthogonal_invariance, check_brute_force,
-              check_golden, check_row_subset]
+              check_golden, check_row_subset, check_brute_force_cross, check_cross_zero_query,
+              check_end_aligned_is_suffix_of_self_attention]

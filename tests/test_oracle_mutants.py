@@ -14,14 +14,16 @@ SRC = os.path.join(ROOT, "oracle", "oracle.c")
 
 MUTANTS = [
     ("dropped scale", "w[j] = J->scale * dot;", "w[j] = dot;"),
-    ("causal mask off by one", "J->causal ? i + 1 : J->N", "J->causal ? i : J->N"),
+    ("causal mask off by one", "i + 1 < nkeys) nkeys = i + 1;", "i < nkeys) nkeys = i;"),
+    ("end-aligned mask without offset", "nkeys = i + 1 + (J->Nk - J->Nq);", "nkeys = i + 1;"),
+    ("end-aligned offset reversed", "nkeys = i + 1 + (J->Nk - J->Nq);", "nkeys = i + 1 + (J->Nq - J->Nk);"),
     ("value used as key", "qi[c] * kh[j * J->d + c]", "qi[c] * vh[j * J->d + c]"),
     ("sign of exponent", "w[j] = exp(w[j] - m);", "w[j] = exp(m - w[j]);"),
     ("missing normalisation", "oi[c] /= l;", "oi[c] /= 1.0;"),
     ("lse without max", "m + log(l)", "log(l)"),
     ("max not subtracted", "w[j] = exp(w[j] - m);", "w[j] = exp(w[j]);"),
-    ("subset row index", "(bh * J->N + i) * J->d", "(bh * J->N + r) * J->d"),
-    ("values from head 0", "J->v + bh * J->N * J->d", "J->v + 0 * J->N * J->d"),
+    ("subset row index", "(bh * J->Nq + i) * J->d", "(bh * J->Nq + r) * J->d"),
+    ("values from head 0", "J->v + bh * J->Nk * J->d", "J->v + 0 * J->Nk * J->d"),
     ("one key dropped", "for (int64_t j = 0; j < nkeys; ++j)\n            for (int64_t c = 0; c < J->d; ++c) oi[c] +=",
      "for (int64_t j = 1; j < nkeys; ++j)\n            for (int64_t c = 0; c < J->d; ++c) oi[c] +="),
 ]

@@ -178,3 +178,15 @@ def test_fp8_pipeline_is_close_to_exact_attention():
     o8, _ = oracle.fp8_pipeline(q, k, v, signs)
     rms = float(np.sqrt(np.mean((o8 - o_ref) ** 2)))
     assert rms < 5e-3
+
+
+def test_rows_without_keys_are_rejected():
+    """A row that sees no key has no softmax: Nk = 0, or the end-aligned mask
+    with more queries than keys."""
+    q, k = np.zeros((1, 1, 4, 2)), np.zeros((1, 1, 3, 2))
+    with pytest.raises(RuntimeError):
+        oracle.attention(q, k, k, causal=2, scale=1.0)
+    with pytest.raises(RuntimeError):
+        oracle.attention(q, np.zeros((1, 1, 0, 2)), np.zeros((1, 1, 0, 2)), scale=1.0)
+    o, lse = oracle.attention(q, k, k, causal=1, scale=1.0)  # rows 3.. see all 3 keys
+    np.testing.assert_allclose(lse[0, 0], np.log([1, 2, 3, 3]), rtol=0, atol=1e-15)
