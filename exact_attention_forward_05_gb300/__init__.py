@@ -25,12 +25,22 @@ __all__ = ["attn_fwd", "attn_fwd_host", "fp8_prepare", "attn_fwd_fp8", "attn_fwd
            "set_wait_timeout_ns", "set_schedule", "debug_bounded_wait", "status_string", "library_path",
            "AttnError", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
            "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "exported_symbols",
-           "LAYOUT_BHND", "LAYOUT_BNHD"]
+           "LAYOUT_BHND", "LAYOUT_BNHD", "CAUSAL_NONE", "CAUSAL_TOP_LEFT", "CAUSAL_BOTTOM_RIGHT"]
 
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_MISALIGNED, ATTN_ERR_CUDA, \
     ATTN_ERR_TIMEOUT = range(6)
 LAYOUT_BHND, LAYOUT_BNHD = 0, 1  # [B, H, N, d] / [B, N, H, d] for q, k, v and o
 _LAYOUTS = {"bhnd": LAYOUT_BHND, "bnhd": LAYOUT_BNHD}
+CAUSAL_NONE, CAUSAL_TOP_LEFT, CAUSAL_BOTTOM_RIGHT = 0, 1, 2
+_CAUSAL_NAMES = {"none": CAUSAL_NONE, "top_left": CAUSAL_TOP_LEFT, "bottom_right": CAUSAL_BOTTOM_RIGHT}
+
+
+def _causal_mode(causal) -> int:
+    """False / True / 0 / 1 / 2 or a name in _CAUSAL_NAMES -> CAUSAL_*."""
+    mode = _CAUSAL_NAMES.get(causal, -1) if isinstance(causal, str) else int(causal)
+    if mode not in (CAUSAL_NONE, CAUSAL_TOP_LEFT, CAUSAL_BOTTOM_RIGHT):
+        raise ValueError("causal must be False, True, 'top_left' or 'bottom_right'")
+    return mode
 ATTN_FP16, ATTN_BF16 = 0, 1
 _DTYPES = {torch.float16: ATTN_FP16, torch.bfloat16: ATTN_BF16}
 
@@ -61,7 +71,7 @@ def _load():
                                      ctypes.c_uint64, ctypes.c_size_t)
             lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp]
             lib.attn_fwd.restype = i32
-            lib.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, i32, vp]
+            lib.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, i32, vp]
             lib.attn_fwd_ex.restype = i32
             lib.attn_fwd_host_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
             lib.attn_fwd_host_workspace_bytes.restype = sz
@@ -130,22 +140,42 @@ def _shape_of(q, k, v):
     return tuple(int(s) for s in q.shape)
 
 
-def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+def _qkv_shapes(q, k, v, layout):
+    """(B, H, Nq, Nk, d) of q [B, H, Nq, d] and k, v [B, H, Nk, d] (or the
+    [B, N, H, d] forms)."""
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape:
+        raise ValueError("q, k, v must be 4-D, k and v of one shape")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in _DTYPES:
+        raise ValueError("q, k, v must all be float16 or all bfloat16")
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous")
+    if layout == "bnhd":
+        (B, Nq, H, d), (Bk, Nk, Hk, dk) = q.shape, k.shape
+    else:
+        (B, H, Nq, d), (Bk, Hk, Nk, dk) = q.shape, k.shape
+    if (B, H, d) != (Bk, Hk, dk):
+        raise ValueError("q, k, v must share B, H and d")
+    return int(B), int(H), int(Nq), int(Nk), int(d)
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal=False,
              scale: float | None = None, out: torch.Tensor | None = None,
              lse: torch.Tensor | None = None, return_lse: bool = True, stream=None,
              layout: str = "bhnd"):
     """Exact attention forward on CUDA tensors (fp16 or bf16).
 
-    ``layout`` is "bhnd" (q, k, v, o are [B, H, N, d]) or "bnhd" ([B, N, H, d],
-    no transpose needed).  Returns (O, lse) with O like q and lse float32
-    [B, H, N] in either layout (None when ``return_lse`` is false and no
-    ``lse`` buffer is given).
+    q: [B, H, Nq, d], k, v: [B, H, Nk, d]; with ``layout="bnhd"`` they are
+    [B, Nq, H, d] and [B, Nk, H, d] (no transpose needed).  ``causal``: False,
+    True (query i sees keys j <= i) or "bottom_right" (query i sees keys
+    j <= i + Nk - Nq: the queries are the last Nq positions).  Returns (O, lse)
+    with O like q and lse float32 [B, H, Nq] in either layout (None when
+    ``return_lse`` is false and no ``lse`` buffer is given).
     """
     if layout not in _LAYOUTS:
         raise ValueError("layout must be 'bhnd' or 'bnhd'")
-    B, H, N, d = _shape_of(q, k, v)
-    if layout == "bnhd":
-        H, N = N, H
+    mode = _causal_mode(causal)
+    B, H, N, Nk, d = _qkv_shapes(q, k, v, layout)
     if not (q.is_cuda and k.device == q.device and v.device == q.device):
         raise ValueError("q, k, v must be CUDA tensors on one device")
     if scale is None:
@@ -162,8 +192,8 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
         raise ValueError("lse must be a contiguous float32 [B, H, N] tensor on q's device")
     with torch.cuda.device(q.device):
         st = _load().attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                                 None if lse is None else lse.data_ptr(), B, H, N, d,
-                                 int(bool(causal)), float(scale), _DTYPES[q.dtype], _LAYOUTS[layout],
+                                 None if lse is None else lse.data_ptr(), B, H, N, Nk, d,
+                                 mode, float(scale), _DTYPES[q.dtype], _LAYOUTS[layout],
                                  _stream_handle(stream, q.device))
     _check(st, "attn_fwd")
     return out, lse

@@ -266,6 +266,6 @@ ATTN_EXPORT attn_status attn_fwd_fp8(const void* q8, const void* k8, const void*
   const int nblk = (N + kQuantRows - 1) / kQuantRows;
   prm.scale_bh_stride = per_tensor ? 0 : nblk;
   prm.scale_blk_stride = per_tensor ? 0 : 1;
-  return attn_kernel::launch_fwd<kHeadDim, KIND_E4M3>(q8, k8, v8, prm, B, H, N, scale,
+  return attn_kernel::launch_fwd<kHeadDim, KIND_E4M3>(q8, k8, v8, prm, B, H, N, N, scale,
                                                       static_cast<cudaStream_t>(stream));
 }

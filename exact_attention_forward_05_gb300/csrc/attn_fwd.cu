@@ -15,13 +15,14 @@ namespace {
 
 template <int D, int KIND>
 attn_status launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                   int N, int causal, float scale, int layout, cudaStream_t stream) {
+                   int Nq, int Nk, int causal, float scale, int layout, cudaStream_t stream) {
   FwdParams prm{};
   prm.o = o;
   prm.lse = lse;
-  prm.causal = causal ? 1 : 0;
+  prm.causal = causal != ATTN_CAUSAL_NONE;
+  prm.causal_off = causal == ATTN_CAUSAL_BOTTOM_RIGHT ? Nk - Nq : 0;
   prm.layout = layout;
-  return attn_kernel::launch_fwd<D, KIND>(q, k, v, prm, B, H, N, scale, stream);
+  return attn_kernel::launch_fwd<D, KIND>(q, k, v, prm, B, H, Nq, Nk, scale, stream);
 }
 
 __global__ void debug_wait_kernel(uint64_t timeout_ns) {
@@ -57,6 +58,10 @@ attn_status check_args(const void* q, const void* k, const void* v, const void* 
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Longest query or key sequence attn_fwd_ex takes: row and key indices plus a
+// tile stay inside int arithmetic in the kernel.
+constexpr int kMaxRows = 1 << 30;
+
 }  // namespace
 
 namespace attn_internal {
@@ -64,27 +69,34 @@ cudaError_t fwd_status_exchange(unsigned int* out) { return attn_kernel::status_
 }  // namespace attn_internal
 
 ATTN_EXPORT attn_status attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                                    int H, int N, int d, int causal, float scale, attn_dtype dtype,
-                                    int layout, void* stream) {
+                                    int H, int Nq, int Nk, int d, int causal, float scale,
+                                    attn_dtype dtype, int layout, void* stream) {
   if (layout != ATTN_LAYOUT_BHND && layout != ATTN_LAYOUT_BNHD) return ATTN_ERR_INVALID_ARG;
-  attn_status st = check_args(q, k, v, o, lse, B, H, N, d, scale, dtype);
-  if (st != ATTN_OK || static_cast<int64_t>(B) * H * N == 0) return st;
+  if (causal != ATTN_CAUSAL_NONE && causal != ATTN_CAUSAL_TOP_LEFT && causal != ATTN_CAUSAL_BOTTOM_RIGHT)
+    return ATTN_ERR_INVALID_ARG;
+  if (Nk < 0) return ATTN_ERR_INVALID_ARG;
+  if (Nq > kMaxRows || Nk > kMaxRows) return ATTN_ERR_UNSUPPORTED;
+  attn_status st = check_args(q, k, v, o, lse, B, H, Nq, d, scale, dtype);
+  if (st != ATTN_OK || static_cast<int64_t>(B) * H * Nq == 0) return st;
+  // Every query row must see at least one key.
+  if (Nk == 0 || (causal == ATTN_CAUSAL_BOTTOM_RIGHT && Nq > Nk)) return ATTN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool bf = dtype == ATTN_BF16;
   switch (d) {
-    case 64: return bf ? launch<64, KIND_BF16>(q, k, v, o, lse, B, H, N, causal, scale, layout, s)
-                       : launch<64, KIND_F16>(q, k, v, o, lse, B, H, N, causal, scale, layout, s);
-    case 128: return bf ? launch<128, KIND_BF16>(q, k, v, o, lse, B, H, N, causal, scale, layout, s)
-                        : launch<128, KIND_F16>(q, k, v, o, lse, B, H, N, causal, scale, layout, s);
-    default: return bf ? launch<256, KIND_BF16>(q, k, v, o, lse, B, H, N, causal, scale, layout, s)
-                       : launch<256, KIND_F16>(q, k, v, o, lse, B, H, N, causal, scale, layout, s);
+    case 64: return bf ? launch<64, KIND_BF16>(q, k, v, o, lse, B, H, Nq, Nk, causal, scale, layout, s)
+                       : launch<64, KIND_F16>(q, k, v, o, lse, B, H, Nq, Nk, causal, scale, layout, s);
+    case 128: return bf ? launch<128, KIND_BF16>(q, k, v, o, lse, B, H, Nq, Nk, causal, scale, layout, s)
+                        : launch<128, KIND_F16>(q, k, v, o, lse, B, H, Nq, Nk, causal, scale, layout, s);
+    default: return bf ? launch<256, KIND_BF16>(q, k, v, o, lse, B, H, Nq, Nk, causal, scale, layout, s)
+                       : launch<256, KIND_F16>(q, k, v, o, lse, B, H, Nq, Nk, causal, scale, layout, s);
   }
 }
 
 ATTN_EXPORT attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                                  int H, int N, int d, int causal, float scale, attn_dtype dtype,
                                  void* stream) {
-  return attn_fwd_ex(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, ATTN_LAYOUT_BHND, stream);
+  return attn_fwd_ex(q, k, v, o, lse, B, H, N, N, d, causal ? ATTN_CAUSAL_TOP_LEFT : ATTN_CAUSAL_NONE,
+                     scale, dtype, ATTN_LAYOUT_BHND, stream);
 }
 
 namespace {

@@ -137,10 +137,12 @@ struct Cfg {
 struct FwdParams {
   void* o;
   float* lse;
-  int BH, N;
-  int H;       // heads: unit head index bh = b * H + h
-  int layout;  // ATTN_LAYOUT_BHND or ATTN_LAYOUT_BNHD, of q, k, v and o
+  int BH, N;      // N: query rows per head
+  int Nk;         // keys per head
+  int H;          // heads: unit head index bh = b * H + h
+  int layout;     // ATTN_LAYOUT_BHND or ATTN_LAYOUT_BNHD, of q, k, v and o
   int causal;
+  int causal_off; // causal: query i sees keys j <= i + causal_off (>= 0)
   float sl2;  // scale * log2(e)
   int units_per_head;
   int num_units;   // work entries: [0, full_units) whole units, then half units
@@ -193,14 +195,14 @@ __device__ __forceinline__ Unit decode_unit(int e, const FwdParams& p) {
     qu = u % p.units_per_head;
   }
   w.m0 = qu * kBM * NQ + (half > 0 ? kBM : 0);
-  w.nkb = (p.N + kBN - 1) / kBN;
+  w.nkb = (p.Nk + kBN - 1) / kBN;
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int r0 = w.m0 + kBM * t;
     if (t >= NQ || r0 >= p.N || (half >= 0 && t > 0))
       w.nb[t] = 0;
     else
-      w.nb[t] = p.causal ? min(w.nkb, r0 / kBN + 1) : w.nkb;
+      w.nb[t] = p.causal ? min(w.nkb, (r0 + kBM - 1 + p.causal_off) / kBN + 1) : w.nkb;
   }
   return w;
 }
@@ -524,7 +526,8 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
       if (nb == 0) continue;
       const int tile_row0 = w.m0 + wg * kBM;
       const int qi = tile_row0 + row;                  // query row of this thread
-      const int diag = tile_row0 / kBN;                // key block holding the diagonal
+      // First key block with a key some row of the tile must not see.
+      const int mask_from = (tile_row0 + p.causal_off + 1) / kBN;
       float m_used = -INFINITY, l = 0.f;
       // FP8: query-block scale and the largest V scale of the blocks visited.
       float c_q = p.sl2, sv_max = 1.f;
@@ -562,12 +565,12 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         reg_pin(s[2]);
         reg_pin(s[3]);
 
-        const bool masked = (p.causal && j == diag) || (j == w.nkb - 1 && (p.N % kBN) != 0);
+        const bool masked = (p.causal && j >= mask_from) || (j == w.nkb - 1 && (p.Nk % kBN) != 0);
         float mblk;
         if (masked) {
           // Scale first, then mask: t = c*s for visible keys, -inf otherwise.
           const int key0 = j * kBN;
-          const int kmax = p.causal ? min(qi, p.N - 1) : p.N - 1;  // last visible key
+          const int kmax = p.causal ? min(qi + p.causal_off, p.Nk - 1) : p.Nk - 1;  // last visible key
           float mx = -INFINITY;
 #pragma unroll
           for (int c = 0; c < 4; ++c)
@@ -754,7 +757,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
 // once per device, and launch one CTA per SM (or per unit, if fewer).
 template <int D, int KIND>
 attn_status launch_fwd(const void* q, const void* k, const void* v, FwdParams prm, int B, int H,
-                       int N, float scale, cudaStream_t stream) {
+                       int N, int Nk, float scale, cudaStream_t stream) {
   using C = Cfg<D, KIND>;
   const CUtensorMapDataType dt = KIND == KIND_E4M3   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                  : KIND == KIND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -762,19 +765,20 @@ attn_status launch_fwd(const void* q, const void* k, const void* v, FwdParams pr
   const uint64_t BH = static_cast<uint64_t>(B) * H;
   CUtensorMap mq, mk, mv, mo;
   const CUtensorMapDataType dto = KIND == KIND_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  // {d, N, H, B} for [B, H, N, d], {d, H, N, B} for [B, N, H, d]; the box is
-  // box_x elements of `rows` consecutive rows of one head.
+  // {d, N, H, B} for [B, H, N, d], {d, H, N, B} for [B, N, H, d], N being the
+  // query length for Q and O and the key length for K and V; the box is box_x
+  // elements of `rows` consecutive rows of one head.
   const bool bnhd = prm.layout == ATTN_LAYOUT_BNHD;
   auto encode = [&](CUtensorMap* m, CUtensorMapDataType t, const void* base, uint64_t elem, uint32_t box_x,
-                    uint32_t rows) {
-    const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(bnhd ? H : N),
-                              static_cast<uint64_t>(bnhd ? N : H), static_cast<uint64_t>(B)};
+                    uint32_t rows, int len) {
+    const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(bnhd ? H : len),
+                              static_cast<uint64_t>(bnhd ? len : H), static_cast<uint64_t>(B)};
     const uint64_t strides[3] = {D * elem, dims[1] * D * elem, dims[2] * dims[1] * D * elem};
     const uint32_t box[4] = {box_x, bnhd ? 1u : rows, bnhd ? rows : 1u, 1u};
     return attn_internal::encode_tmap_4d(m, t, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
   };
-  if (!encode(&mq, dt, q, C::ELEM, C::CHUNK_ELEMS, kBM) || !encode(&mk, dt, k, C::ELEM, C::CHUNK_ELEMS, kBN) ||
-      !encode(&mv, dt, v, C::ELEM, C::CHUNK_ELEMS, kBN) || !encode(&mo, dto, prm.o, 2, 64, kBM))
+  if (!encode(&mq, dt, q, C::ELEM, C::CHUNK_ELEMS, kBM, N) || !encode(&mk, dt, k, C::ELEM, C::CHUNK_ELEMS, kBN, Nk) ||
+      !encode(&mv, dt, v, C::ELEM, C::CHUNK_ELEMS, kBN, Nk) || !encode(&mo, dto, prm.o, 2, 64, kBM, N))
     return ATTN_ERR_CUDA;
 
   static int configured_for[64] = {0};  // per device: dynamic shared memory attribute set
@@ -790,6 +794,7 @@ attn_status launch_fwd(const void* q, const void* k, const void* v, FwdParams pr
   prm.BH = static_cast<int>(BH);
   prm.H = H;
   prm.N = N;
+  prm.Nk = Nk;
   prm.sl2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.units_per_head = (N + kBM * C::NQ - 1) / (kBM * C::NQ);
   const int units = prm.units_per_head * prm.BH;

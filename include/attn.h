@@ -19,7 +19,8 @@
  * Conventions shared by every entry point:
  *  - Layout: Q, K, V, O are contiguous [B, H, N, d] (row-major, d innermost);
  *    self-attention, so queries and keys share N.  lse is contiguous [B, H, N].
- *    attn_fwd_ex also takes Q, K, V, O as contiguous [B, N, H, d].
+ *    attn_fwd_ex also takes Q, K, V, O as contiguous [B, N, H, d], and
+ *    queries and keys of different lengths (Nq, Nk).
  *  - Device pointers are CUDA device addresses on the current device; every
  *    tensor base must be 16-byte aligned (lse: 4-byte aligned).
  *  - Ownership: the caller owns every buffer.  The library never allocates
@@ -31,8 +32,9 @@
  *    across this boundary.  A kernel whose internal wait runs past its time
  *    limit stops cleanly and records ATTN_ERR_TIMEOUT in the device status
  *    word, read with attn_get_device_status().
- *  - Causal mask: query i sees keys j <= i (queries and keys aligned at 0).
- *    Keys beyond N never contribute; rows beyond N are never written.
+ *  - Causal mask: query i sees keys j <= i (queries and keys aligned at 0;
+ *    attn_fwd_ex can align them at the end instead).  Keys beyond N never
+ *    contribute; rows beyond N are never written.
  */
 #ifndef GB300_ATTN_H
 #define GB300_ATTN_H
@@ -59,6 +61,12 @@ typedef enum { ATTN_FP16 = 0, ATTN_BF16 = 1 } attn_dtype;
 #define ATTN_LAYOUT_BHND 0 /* [B, H, N, d]: each head's rows contiguous */
 #define ATTN_LAYOUT_BNHD 1 /* [B, N, H, d]: each token's heads contiguous */
 
+/* Causal mask of attn_fwd_ex over Nq queries and Nk keys (the two coincide when
+ * Nq = Nk, where they are the causal mask of self-attention). */
+#define ATTN_CAUSAL_NONE 0         /* every key visible */
+#define ATTN_CAUSAL_TOP_LEFT 1     /* query i sees keys j <= i */
+#define ATTN_CAUSAL_BOTTOM_RIGHT 2 /* query i sees keys j <= i + Nk - Nq (requires Nq <= Nk) */
+
 /*
  * attn_fwd -- exact attention forward, 16-bit inputs and output.
  *
@@ -79,16 +87,30 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
                      int N, int d, int causal, float scale, attn_dtype dtype, void* stream);
 
 /*
- * attn_fwd_ex -- attn_fwd with the memory layout of Q, K, V and O chosen by
- * `layout`: ATTN_LAYOUT_BHND ([B, H, N, d], exactly attn_fwd) or
- * ATTN_LAYOUT_BNHD ([B, N, H, d], the layout a projection of [B, N, H*d]
- * activations gives, so that no transpose is needed).  lse is [B, H, N] either
- * way.  The results are the same values, element for element, as attn_fwd on
- * the inputs transposed to [B, H, N, d].  Any other `layout` returns
- * ATTN_ERR_INVALID_ARG; the other arguments, rules and errors are attn_fwd's.
+ * attn_fwd_ex -- attn_fwd generalised to Nq queries over Nk keys and to a
+ * second memory layout.
+ *
+ *   q, o   : Nq rows per head; k, v : Nk rows per head.
+ *   layout : ATTN_LAYOUT_BHND (q, o [B, H, Nq, d]; k, v [B, H, Nk, d]) or
+ *            ATTN_LAYOUT_BNHD (q, o [B, Nq, H, d]; k, v [B, Nk, H, d], the
+ *            layout a projection of [B, N, H*d] activations gives, so that no
+ *            transpose is needed).  lse is [B, H, Nq] either way.
+ *   causal : ATTN_CAUSAL_NONE, ATTN_CAUSAL_TOP_LEFT or ATTN_CAUSAL_BOTTOM_RIGHT
+ *            (the queries are the last Nq of Nk positions: cross-attention
+ *            over a key prefix, chunked prefill).
+ *
+ * The FlashAttention pages define the causal mask for self-attention only;
+ * for Nq != Nk both alignments above are readings of it.  With Nq = Nk and
+ * layout BHND this is attn_fwd, bit for bit; BNHD gives the same values,
+ * element for element, as BHND on the transposed inputs.
+ * Errors (ATTN_ERR_INVALID_ARG, nothing launched): a `layout` or `causal`
+ * value not listed; Nk < 0; when B*H*Nq > 0, Nk == 0 or BOTTOM_RIGHT with
+ * Nq > Nk (a query row would see no key).  ATTN_ERR_UNSUPPORTED: Nq or Nk
+ * above 2^30.  Otherwise attn_fwd's rules and errors, with N read as Nq.
  */
 attn_status attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                        int N, int d, int causal, float scale, attn_dtype dtype, int layout, void* stream);
+                        int Nq, int Nk, int d, int causal, float scale, attn_dtype dtype, int layout,
+                        void* stream);
 
 /*
  * attn_fwd_host_workspace_bytes -- device workspace (bytes) attn_fwd_host needs

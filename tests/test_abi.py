@@ -58,20 +58,37 @@ def test_validation_before_launch(lib):
     assert _fwd(lib, B=65536, H=65536) == attn.ATTN_ERR_INVALID_ARG
 
 
+def _fwd_ex(lib, layout=0, causal=0, **kw):
+    a = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, B=1, H=1, Nq=8, Nk=8, d=128)
+    a.update(kw)
+    return lib.attn_fwd_ex(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"], a["Nk"],
+                           a["d"], causal, 0.1, attn.ATTN_BF16, layout, None)
+
+
 def test_layout_argument(lib):
-    def fwd_ex(layout, **kw):
-        a = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, B=1, H=1, N=8, d=128)
-        a.update(kw)
-        return lib.attn_fwd_ex(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["d"],
-                               0, 0.1, attn.ATTN_BF16, layout, None)
     assert attn.LAYOUT_BHND == 0 and attn.LAYOUT_BNHD == 1
     for bad in (2, -1, 7):
-        assert fwd_ex(bad) == attn.ATTN_ERR_INVALID_ARG
+        assert _fwd_ex(lib, layout=bad) == attn.ATTN_ERR_INVALID_ARG
     # The layout check comes first; the remaining checks are attn_fwd's.
-    assert fwd_ex(2, N=0) == attn.ATTN_ERR_INVALID_ARG
-    assert fwd_ex(attn.LAYOUT_BNHD, d=96) == attn.ATTN_ERR_UNSUPPORTED
-    assert fwd_ex(attn.LAYOUT_BNHD, q=0x1008) == attn.ATTN_ERR_MISALIGNED
-    assert fwd_ex(attn.LAYOUT_BNHD, N=0, q=None, k=None, v=None, o=None) == attn.ATTN_OK
+    assert _fwd_ex(lib, layout=2, Nq=0) == attn.ATTN_ERR_INVALID_ARG
+    assert _fwd_ex(lib, layout=attn.LAYOUT_BNHD, d=96) == attn.ATTN_ERR_UNSUPPORTED
+    assert _fwd_ex(lib, layout=attn.LAYOUT_BNHD, q=0x1008) == attn.ATTN_ERR_MISALIGNED
+    assert _fwd_ex(lib, layout=attn.LAYOUT_BNHD, Nq=0, q=None, k=None, v=None, o=None) == attn.ATTN_OK
+
+
+def test_query_key_lengths_and_causal_modes(lib):
+    assert (attn.CAUSAL_NONE, attn.CAUSAL_TOP_LEFT, attn.CAUSAL_BOTTOM_RIGHT) == (0, 1, 2)
+    for bad in (3, -1):
+        assert _fwd_ex(lib, causal=bad) == attn.ATTN_ERR_INVALID_ARG
+    assert _fwd_ex(lib, Nk=-1) == attn.ATTN_ERR_INVALID_ARG
+    for causal in (0, 1, 2):  # no keys: no softmax
+        assert _fwd_ex(lib, causal=causal, Nk=0) == attn.ATTN_ERR_INVALID_ARG
+    # Aligned at the end with more queries than keys: rows without a key.
+    assert _fwd_ex(lib, causal=2, Nq=9, Nk=8) == attn.ATTN_ERR_INVALID_ARG
+    # No query rows: nothing to do, whatever Nk is.
+    assert _fwd_ex(lib, causal=2, Nq=0, Nk=0, q=None, k=None, v=None, o=None) == attn.ATTN_OK
+    assert _fwd_ex(lib, causal=1, Nq=9, Nk=8, d=96) == attn.ATTN_ERR_UNSUPPORTED
+    assert _fwd_ex(lib, causal=2, Nq=3, Nk=8, k=0x2004) == attn.ATTN_ERR_MISALIGNED
 
 
 def test_python_layout_and_out_checks(lib):
@@ -81,6 +98,12 @@ def test_python_layout_and_out_checks(lib):
         attn.attn_fwd(q, q, q, layout="nhd")
     with pytest.raises(ValueError):  # host tensors
         attn.attn_fwd(q, q, q, layout="bnhd")
+    for bad in ("diagonal", 3):
+        with pytest.raises(ValueError):
+            attn.attn_fwd(q, q, q, causal=bad)
+    k = torch.zeros(1, 8, 5, 32, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):  # head dims differ
+        attn.attn_fwd(q, k, k)
 
 
 def test_empty_problem_launches_nothing(lib):

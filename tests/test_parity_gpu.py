@@ -210,3 +210,76 @@ def test_bnhd_layout_many_units():
         torch.cuda.synchronize()
         assert torch.equal(o.transpose(1, 2), o_ref) and torch.equal(lse, lse_ref), causal
     assert attn.device_status() == attn.ATTN_OK
+
+
+def _cross_inputs(B, H, Nq, Nk, d, dtype, seed):
+    q = parity.inputs(B, H, Nq, d, dtype, seed=seed)[0]
+    _, k, v = parity.inputs(B, H, Nk, d, dtype, seed=seed + 1)
+    return q, k, v
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("Nq,Nk", [(100, 300), (300, 129), (129, 700), (1, 257), (383, 385)])
+def test_query_and_key_lengths_differ(d, Nq, Nk):
+    """Nq != Nk, every row against the oracle, for no mask and both causal
+    alignments (the end-aligned one only where every row sees a key); the
+    output buffer is one batch longer and NaN-filled: rows past Nq stay unwritten."""
+    B, H = 2, 2
+    q, k, v = _cross_inputs(B, H, Nq, Nk, d, "bf16", seed=53 + d + Nq)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    for causal in (0, 1, 2):
+        if causal == 2 and Nq > Nk:
+            continue
+        big = torch.full((B + 1, H, Nq, d), float("nan"), dtype=qd.dtype, device="cuda")
+        o, lse = attn.attn_fwd(qd, kd, vd, causal=causal, out=big[:B])
+        torch.cuda.synchronize()
+        assert torch.isnan(big[B]).all(), "rows past the end written"
+        m = parity.metrics(o, lse, *oracle.attention(q, k, v, causal=causal, scale=d ** -0.5))
+        parity.assert_close(m, what=f"Nq={Nq} Nk={Nk} d={d} causal={causal}")
+    assert attn.device_status() == attn.ATTN_OK
+
+
+def test_query_and_key_lengths_bnhd_and_fp16():
+    """Nq != Nk through the [B, N, H, d] layout, in bf16 and fp16: the same
+    bits as the [B, H, N, d] launch on transposed inputs, and the oracle."""
+    B, H, Nq, Nk, d = 2, 3, 200, 600, 128
+    for dtype in ("bf16", "fp16"):
+        q, k, v = _cross_inputs(B, H, Nq, Nk, d, dtype, seed=57)
+        for causal in (0, 1, 2):
+            o_ref, l_ref = attn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal)
+            qt, kt, vt = (t.transpose(1, 2).contiguous().cuda() for t in (q, k, v))
+            o, lse = attn.attn_fwd(qt, kt, vt, causal=causal, layout="bnhd")
+            torch.cuda.synchronize()
+            assert torch.equal(o.transpose(1, 2), o_ref) and torch.equal(lse, l_ref), (dtype, causal)
+            m = parity.metrics(o_ref, l_ref, *oracle.attention(q, k, v, causal=causal, scale=d ** -0.5))
+            parity.assert_close(m, what=f"{dtype} causal={causal}")
+    assert attn.device_status() == attn.ATTN_OK
+
+
+def test_end_aligned_mask_equals_causal_at_equal_lengths():
+    """With Nq = Nk the two causal alignments are one mask: identical bits."""
+    q, k, v = (t.cuda() for t in parity.inputs(2, 4, 1000, 128, "bf16", seed=59))
+    o1, l1 = attn.attn_fwd(q, k, v, causal=True)
+    o2, l2 = attn.attn_fwd(q, k, v, causal="bottom_right")
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_chunked_prefill_matches_full_causal():
+    """Queries split into chunks, each attending to all keys up to its end with
+    the end-aligned mask, give the rows of one causal self-attention launch
+    (the same keys and masks per row; sampled rows also against the oracle)."""
+    B, H, N, d = 1, 4, 2048, 128
+    q, k, v = (t.cuda() for t in parity.inputs(B, H, N, d, "bf16", seed=61))
+    o_full, l_full = attn.attn_fwd(q, k, v, causal=True)
+    for lo, hi in ((0, 256), (256, 640), (640, 1100), (1100, 2048)):
+        qc = q[:, :, lo:hi].contiguous()
+        kc, vc = k[:, :, :hi].contiguous(), v[:, :, :hi].contiguous()
+        oc, lc = attn.attn_fwd(qc, kc, vc, causal="bottom_right")
+        torch.cuda.synchronize()
+        assert (oc.float() - o_full[:, :, lo:hi].float()).abs().max().item() <= 2 ** -7, (lo, hi)
+        assert (lc - l_full[:, :, lo:hi]).abs().max().item() <= 1e-4, (lo, hi)
+    rows = [0, 255, 256, 1099, 1100, 2047]
+    o_ref, l_ref = oracle.attention(q.cpu()[:, :1], k.cpu()[:, :1], v.cpu()[:, :1], causal=True, scale=d ** -0.5, rows=rows)
+    m = parity.metrics(o_full[:, :1, rows], l_full[:, :1, rows], o_ref, l_ref)
+    parity.assert_close(m, what="full causal sampled rows")
