@@ -16,6 +16,10 @@ Definitions (each cited where it is computed, in ``oracle.c``):
 * ``hadamard_rotate``: x -> (x * sigma) H_d / sqrt(d) with the Sylvester
   Hadamard matrix, the random-sign rotation of "Incoherent Processing for FP8
   Accuracy" (FlashAttention-3 podcast page).
+* ``rotary``: the rotary position embedding that the same section names as the
+  memory-bound step the rotation is fused into; the pages do not define it, so
+  it is RoFormer's pairwise rotation by position-dependent angles, with the
+  angles given as cos / sin tables and either pairing convention.
 * ``block_quantize``: per-block (or per-tensor) amax scaling to E4M3, the block
   quantisation of the comrad404 review, "Метод", item 3.
 * ``fp8_pipeline``: the composition of the three steps above followed by exact
@@ -76,6 +80,8 @@ def _load():
             lib.oracle_hadamard_entry.restype = i32
             lib.oracle_hadamard_rotate.argtypes = [dp, dp, dp, i64, i64, i64, i64]
             lib.oracle_hadamard_rotate.restype = i32
+            lib.oracle_rotary.argtypes = [dp, dp, dp, dp, i64, i64, i64, i32]
+            lib.oracle_rotary.restype = i32
             lib.oracle_block_quantize.argtypes = [dp, dp, dp, i64, i64, i64, i64, i32]
             lib.oracle_block_quantize.restype = i32
             _lib = lib
@@ -158,6 +164,28 @@ def hadamard_rotate(x, signs) -> np.ndarray:
     return out
 
 
+def rotary(x, cos, sin, interleaved: bool = False) -> np.ndarray:
+    """x [B, H, N, d] -> the rotary position embedding of every row, float64;
+    cos, sin: [N, d/2] tables (float32 values), pair i = (2i, 2i+1) when
+    ``interleaved`` else (i, i + d/2)."""
+    a = _f64(x)
+    B, H, N, d = a.shape
+    c = np.ascontiguousarray(_np32(cos))
+    s = np.ascontiguousarray(_np32(sin))
+    if c.shape != (N, d // 2) or s.shape != (N, d // 2):
+        raise ValueError("cos, sin must be [N, d/2]")
+    out = np.empty_like(a)
+    st = _load().oracle_rotary(_ptr(a), _ptr(c), _ptr(s), _ptr(out), B * H, N, d, int(bool(interleaved)))
+    if st != 0:
+        raise RuntimeError(f"oracle_rotary failed with status {st}")
+    return out
+
+
+def _np32(t) -> np.ndarray:
+    t = t.cpu().numpy() if hasattr(t, "cpu") else np.asarray(t)
+    return t.astype(np.float32)
+
+
 def block_quantize(x, block: int = QUANT_BLOCK, per_tensor: bool = False):
     """E4M3 codes [B, H, N, d] and float32 scales [B, H, ceil(N/block)] (or [1])."""
     a = _f64(x)
@@ -183,10 +211,13 @@ def dequantize(codes, scales, block: int = QUANT_BLOCK) -> np.ndarray:
 
 
 def fp8_pipeline(q, k, v, signs=None, causal: bool = False, scale: float | None = None,
-                 per_tensor: bool = False, rows=None, block: int = QUANT_BLOCK):
-    """Rotate Q and K (if ``signs``), quantise Q, K, V to E4M3, then exact attention
-    on the dequantised operands.  Returns (O, lse) like ``attention``."""
+                 per_tensor: bool = False, rows=None, block: int = QUANT_BLOCK, rope=None):
+    """Rotary embedding of Q and K (if ``rope`` = (cos, sin, interleaved)), their
+    Hadamard rotation (if ``signs``), E4M3 quantisation of Q, K, V, then exact
+    attention on the dequantised operands.  Returns (O, lse) like ``attention``."""
     qf, kf, vf = _f64(q), _f64(k), _f64(v)
+    if rope is not None:
+        qf, kf = (rotary(t, rope[0], rope[1], rope[2]) for t in (qf, kf))
     if signs is not None:
         qf, kf = hadamard_rotate(qf, signs), hadamard_rotate(kf, signs)
     deq = []

@@ -208,6 +208,34 @@ ORACLE_API int oracle_hadamard_rotate(const double *x, const int8_t *signs, doub
     return 0;
 }
 
+/* ------------------------------------------------------------ rotary */
+
+/* Rotary position embedding (RoFormer: each pair of features of the row at
+ * position n is rotated by the angle n * theta_i), with the angles given as
+ * tables: cos_t, sin_t [N, d/2] (float32, widened exactly), entry (n, i) for
+ * pair i of row n.  Pair i is (2i, 2i+1) when interleaved != 0, else
+ * (i, i + d/2).  A pair (a, b) becomes (a cos - b sin, a sin + b cos).
+ * x, out: [BH, N, d] float64. */
+ORACLE_API int oracle_rotary(const double *x, const float *cos_t, const float *sin_t, double *out,
+                             int64_t BH, int64_t N, int64_t d, int interleaved) {
+    if (d < 2 || (d & 1)) return 2;
+    const int64_t half = d / 2;
+    for (int64_t bh = 0; bh < BH; ++bh)
+        for (int64_t n = 0; n < N; ++n) {
+            const double *xr = x + (bh * N + n) * d;
+            double *yr = out + (bh * N + n) * d;
+            for (int64_t i = 0; i < half; ++i) {
+                const int64_t ia = interleaved ? 2 * i : i;
+                const int64_t ib = interleaved ? 2 * i + 1 : i + half;
+                const double c = (double)cos_t[n * half + i], s = (double)sin_t[n * half + i];
+                const double a = xr[ia], b = xr[ib];
+                yr[ia] = a * c - b * s;
+                yr[ib] = a * s + b * c;
+            }
+        }
+    return 0;
+}
+
 /* ------------------------------------------------------ block quantisation */
 
 /* x: [BH, N, d].  For every (bh, block of `block` rows) -- or for the whole

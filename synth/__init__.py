@@ -136,6 +136,17 @@ def hadamard_signs(H: int, d: int, seed: int = 0) -> torch.Tensor:
     return torch.from_numpy(s.reshape(H, d)).contiguous()
 
 
+def rotary_tables(N: int, d: int, base: float = 10000.0, offset: int = 0):
+    """cos / sin tables [N, d/2] float32 of a rotary embedding cache: entry
+    (n, i) of the angle (n + offset) * base^(-2i/d), evaluated in float64 and
+    rounded once.  Deterministic: a caller-side input, like the signs."""
+    pos = np.arange(offset, offset + N, dtype=np.float64)[:, None]
+    inv_freq = base ** (-np.arange(0, d, 2, dtype=np.float64) / d)[None, :]
+    ang = pos * inv_freq
+    return (torch.from_numpy(np.cos(ang).astype(np.float32)).contiguous(),
+            torch.from_numpy(np.sin(ang).astype(np.float32)).contiguous())
+
+
 def sample_rows(N: int, count: int, seed: int = 0, salt: int = 0) -> np.ndarray:
     """``count`` distinct query rows in [0, N), sorted (seeded partial shuffle)."""
     count = min(count, N)

@@ -11,6 +11,29 @@ sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
 from tests import pins  # noqa: E402
 
 
+def main_rotary(lib_path):
+    lib = ctypes.CDLL(lib_path)
+    dp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.oracle_rotary.argtypes = [dp, dp, dp, dp, i64, i64, i64, i32]
+    lib.oracle_rotary.restype = i32
+
+    def rot(x, c, s, interleaved):
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        c, s = (np.ascontiguousarray(t, dtype=np.float32) for t in (c, s))
+        B, H, N, d = x.shape
+        out = np.empty_like(x)
+        p = lambda a: ctypes.c_void_p(a.ctypes.data)
+        assert lib.oracle_rotary(p(x), p(c), p(s), p(out), B * H, N, d, int(interleaved)) == 0
+        return out
+
+    try:
+        pins.check_rotary_complex(rot)
+    except AssertionError:
+        print("failed: check_rotary_complex")
+        return 1
+    return 0
+
+
 def main(lib_path):
     lib = ctypes.CDLL(lib_path)
     i64, dp, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
@@ -44,4 +67,4 @@ def main(lib_path):
 
 
 if __name__ == "__main__":
-    sys.exit(main(sys.argv[1]))
+    sys.exit(main_rotary(sys.argv[1]) if sys.argv[2:] == ["rotary"] else main(sys.argv[1]))

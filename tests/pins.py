@@ -236,6 +236,24 @@ def check_end_aligned_is_suffix_of_self_attention(attn):
     np.testing.assert_allclose(lse, lse_self[:, :, Nk - Nq:], rtol=0, atol=1e-12)
 
 
+def check_rotary_complex(rot):
+    """``rot(x, cos, sin, interleaved) -> out`` against RoFormer's definition: a
+    feature pair read as the complex number a + ib is multiplied by e^{i phi}.
+    Random angles per (position, pair); numpy's complex arithmetic on the same
+    float32 table values."""
+    B, H, N, d = 2, 3, 5, 8
+    x = _rand((B, H, N, d), 80)
+    phi = _rng(81).uniform(-np.pi, np.pi, (N, d // 2))
+    c32, s32 = np.cos(phi).astype(np.float32), np.sin(phi).astype(np.float32)
+    for interleaved in (False, True):
+        out = rot(x, c32, s32, interleaved)
+        ia = np.arange(0, d, 2) if interleaved else np.arange(d // 2)
+        ib = ia + 1 if interleaved else ia + d // 2
+        z = (x[..., ia] + 1j * x[..., ib]) * (c32.astype(np.float64) + 1j * s32.astype(np.float64))
+        np.testing.assert_allclose(out[..., ia], z.real, rtol=0, atol=1e-14)
+        np.testing.assert_allclose(out[..., ib], z.imag, rtol=0, atol=1e-14)
+
+
 def check_golden(attn):
     """Hand-worked examples with exact expected values."""
     with open(os.path.join(GOLDEN, "two_key_softmax.json")) as f:

@@ -29,8 +29,16 @@ MUTANTS = [
 ]
 
 
-@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_mutant_fails_a_pin(tmp_path, name, old, new):
+# Mistakes in the rotary embedding, each caught by the complex-number pin.
+ROTARY_MUTANTS = [
+    ("rotary sign of sin", "yr[ia] = a * c - b * s;", "yr[ia] = a * c + b * s;"),
+    ("rotary cos and sin swapped", "yr[ib] = a * s + b * c;", "yr[ib] = a * c + b * s;"),
+    ("rotary half-split partner", "interleaved ? 2 * i + 1 : i + half", "interleaved ? 2 * i + 1 : i + 1"),
+    ("rotary table row ignored", "cos_t[n * half + i]", "cos_t[i]"),
+]
+
+
+def _run_mutant(tmp_path, old, new, *mode):
     src = open(SRC).read()
     assert src.count(old) == 1, f"mutation site not found once: {old!r}"
     path = tmp_path / "mutant.c"
@@ -38,15 +46,27 @@ def test_mutant_fails_a_pin(tmp_path, name, old, new):
     lib = tmp_path / "libmutant.so"
     subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread", "-D_GNU_SOURCE",
                     str(path), "-o", str(lib), "-lm"], check=True)
-    res = subprocess.run([sys.executable, os.path.join(ROOT, "tests", "_mutant_runner.py"), str(lib)],
-                         capture_output=True, text=True, timeout=300)
+    return subprocess.run([sys.executable, os.path.join(ROOT, "tests", "_mutant_runner.py"), str(lib), *mode],
+                          capture_output=True, text=True, timeout=300)
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_fails_a_pin(tmp_path, name, old, new):
+    res = _run_mutant(tmp_path, old, new)
     assert res.returncode == 1, f"mutant '{name}' survived every pin: {res.stdout}{res.stderr}"
+
+
+@pytest.mark.parametrize("name,old,new", ROTARY_MUTANTS, ids=[m[0] for m in ROTARY_MUTANTS])
+def test_rotary_mutant_fails_the_pin(tmp_path, name, old, new):
+    res = _run_mutant(tmp_path, old, new, "rotary")
+    assert res.returncode == 1, f"mutant '{name}' survived: {res.stdout}{res.stderr}"
 
 
 def test_unmutated_copy_passes_every_pin(tmp_path):
     lib = tmp_path / "libcopy.so"
     subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread", "-D_GNU_SOURCE",
                     SRC, "-o", str(lib), "-lm"], check=True)
-    res = subprocess.run([sys.executable, os.path.join(ROOT, "tests", "_mutant_runner.py"), str(lib)],
-                         capture_output=True, text=True, timeout=300)
-    assert res.returncode == 0, res.stdout + res.stderr
+    for mode in ([], ["rotary"]):
+        res = subprocess.run([sys.executable, os.path.join(ROOT, "tests", "_mutant_runner.py"), str(lib), *mode],
+                             capture_output=True, text=True, timeout=300)
+        assert res.returncode == 0, res.stdout + res.stderr

@@ -190,3 +190,36 @@ def test_rows_without_keys_are_rejected():
         oracle.attention(q, np.zeros((1, 1, 0, 2)), np.zeros((1, 1, 0, 2)), scale=1.0)
     o, lse = oracle.attention(q, k, k, causal=1, scale=1.0)  # rows 3.. see all 3 keys
     np.testing.assert_allclose(lse[0, 0], np.log([1, 2, 3, 3]), rtol=0, atol=1e-15)
+
+
+def test_rotary_is_complex_multiplication():
+    pins.check_rotary_complex(lambda x, c, s, inter: oracle.rotary(x, c, s, interleaved=inter))
+
+
+def test_rotary_zero_angle_is_identity_and_norms_are_kept():
+    x = np.random.default_rng(82).standard_normal((1, 2, 7, 16))
+    one, zero = np.ones((7, 8), np.float32), np.zeros((7, 8), np.float32)
+    for inter in (False, True):
+        np.testing.assert_array_equal(oracle.rotary(x, one, zero, inter), x)
+        c, s = synth.rotary_tables(7, 16, offset=3)
+        y = oracle.rotary(x, c, s, inter)
+        # cos^2 + sin^2 of the float32 table entries is 1 to ~1e-7.
+        np.testing.assert_allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1), rtol=2e-7)
+
+
+def test_rotary_scores_depend_on_relative_position_only():
+    """<R_m q, R_n k> = <R_{m+s} q, R_{n+s} k>: shifting every position by s
+    (tables with an offset) leaves every logit unchanged, up to the float32
+    rounding of the tables."""
+    N, d = 40, 64
+    q = np.random.default_rng(83).standard_normal((1, 1, N, d))
+    k = np.random.default_rng(84).standard_normal((1, 1, N, d))
+    for inter in (False, True):
+        c0, s0 = synth.rotary_tables(N, d, offset=0)
+        c1, s1 = synth.rotary_tables(N, d, offset=57)
+        l0 = oracle.rotary(q, c0, s0, inter)[0, 0] @ oracle.rotary(k, c0, s0, inter)[0, 0].T
+        l1 = oracle.rotary(q, c1, s1, inter)[0, 0] @ oracle.rotary(k, c1, s1, inter)[0, 0].T
+        np.testing.assert_allclose(l1, l0, rtol=0, atol=1e-4)
+        # ... while the logits themselves do change with the relative position.
+        plain = q[0, 0] @ k[0, 0].T
+        assert np.abs(l0 - plain).max() > 1.0
