@@ -352,7 +352,8 @@ def fp8_leg(w, dev, stream, rank, args):
     """The FP8 path on the same shapes with 0.1 % outliers in Q, K, V: the FP8
     attention kernel alone (against the FP8 dense peak = 2 x the measured bf16
     peak, the nominal FP8/BF16 ratio of the tensor cores), the pre-pass
-    (Hadamard rotation + block quantisation, HBM-bound) and the two together;
+    (Hadamard rotation + block quantisation, HBM-bound), the pre-pass with the
+    rotary embedding of Q and K fused in front, and pre-pass + kernel together;
     plus the RMS error against exact attention on sampled rows next to the
     naive per-tensor FP8 baseline."""
     import exact_attention_forward_05_gb300 as attn
@@ -368,6 +369,8 @@ def fp8_leg(w, dev, stream, rank, args):
     l8 = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     scale = d ** -0.5
     prep = lambda: attn.fp8_prepare(qd, kd, vd, signs=signs, out=bufs, stream=stream)
+    rope = tuple(t.to(dev) for t in synth.rotary_tables(N, d))
+    prep_rope = lambda: attn.fp8_prepare(qd, kd, vd, signs=signs, out=bufs, stream=stream, rope=rope)
     fwd = lambda: attn.attn_fwd_fp8(*bufs, causal=w["causal"], scale=scale, out=o8, lse=l8, stream=stream)
     def both():
         prep()
@@ -376,6 +379,7 @@ def fp8_leg(w, dev, stream, rank, args):
     prep()
     t_fwd = time_kernel(fwd, n, 3, stream) / n
     t_prep = time_kernel(prep, n, 3, stream) / n
+    t_prep_rope = time_kernel(prep_rope, n, 3, stream) / n
     t_both = time_kernel(both, n, 3, stream) / n
     if attn.device_status() != attn.ATTN_OK:
         raise RuntimeError("device status after the FP8 leg")
@@ -390,6 +394,7 @@ def fp8_leg(w, dev, stream, rank, args):
                         "peak_source": "2 x measured bf16 burst (nominal FP8 / BF16 dense ratio)",
                         "kernel": "attn_fwd_kernel<128, e4m3>"},
            "prepare_us": round(t_prep * 1e3, 2),
+           "prepare_rotary_us": round(t_prep_rope * 1e3, 2),
            "prepare_gbs": round((3 * q.numel() * 2 + 3 * q.numel() + 3 * B * H * nblk * 4) / (t_prep * 1e-3) / 1e9, 1),
            "pipeline_value": round(fl / (t_both * 1e-3) / 1e12, 2)}
     if rank == 0:

@@ -81,6 +81,9 @@ def _load():
             lib.attn_fp8_prepare.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, i32,
                                              i32, i32, i32, i32, vp]
             lib.attn_fp8_prepare.restype = i32
+            lib.attn_fp8_prepare_rotary.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, i32,
+                                                    vp, vp, i32, i32, i32, i32, i32, vp]
+            lib.attn_fp8_prepare_rotary.restype = i32
             lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
                                          i32, f32, vp]
             lib.attn_fwd_fp8.restype = i32
@@ -236,11 +239,13 @@ FP8_BLOCK = 128  # rows per quantisation scale block
 
 
 def fp8_prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, signs: torch.Tensor | None = None,
-                per_tensor: bool = False, stream=None, out=None):
-    """FP8 pre-pass on CUDA tensors [B, H, N, 128] (fp16 or bf16): random-sign
-    Hadamard rotation of Q and K (when ``signs`` [H, 128] int8 is given) and
-    E4M3 quantisation with one float32 scale per 128 rows of a head (or one per
-    tensor).  Returns (q8, k8, v8, q_scale, k_scale, v_scale); the codes are
+                per_tensor: bool = False, stream=None, out=None, rope=None, rope_interleaved: bool = False):
+    """FP8 pre-pass on CUDA tensors [B, H, N, 128] (fp16 or bf16): rotary
+    embedding of Q and K (when ``rope`` = (cos, sin), float32 [N, 64] CUDA
+    tables; pairs (2i, 2i+1) if ``rope_interleaved`` else (i, i + 64)), then
+    their random-sign Hadamard rotation (when ``signs`` [H, 128] int8 is given)
+    and E4M3 quantisation with one float32 scale per 128 rows of a head (or one
+    per tensor).  Returns (q8, k8, v8, q_scale, k_scale, v_scale); the codes are
     uint8 tensors [B, H, N, 128].  ``out`` may pass those six tensors in."""
     B, H, N, d = _shape_of(q, k, v)
     if not q.is_cuda:
@@ -262,12 +267,20 @@ def fp8_prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, signs: torch.
         if signs.dtype != torch.int8 or tuple(signs.shape) != (H, d):
             raise ValueError("signs must be an int8 [H, d] tensor of +1 / -1")
         signs = signs.to(q.device).contiguous()
+    rc = rs = None
+    if rope is not None:
+        rc, rs = rope
+        for t in (rc, rs):
+            if (t.dtype != torch.float32 or tuple(t.shape) != (N, d // 2) or not t.is_contiguous()
+                    or t.device != q.device):
+                raise ValueError("rope tables must be contiguous float32 [N, d/2] on q's device")
     with torch.cuda.device(q.device):
-        st = _load().attn_fp8_prepare(
+        st = _load().attn_fp8_prepare_rotary(
             q.data_ptr(), k.data_ptr(), v.data_ptr(), _DTYPES[q.dtype],
             *(c.data_ptr() for c in codes), *(sc.data_ptr() for sc in scales),
-            None if signs is None else signs.data_ptr(), int(bool(per_tensor)), B, H, N, d,
-            _stream_handle(stream, q.device))
+            None if signs is None else signs.data_ptr(), int(bool(per_tensor)),
+            None if rc is None else rc.data_ptr(), None if rs is None else rs.data_ptr(),
+            int(bool(rope_interleaved)), B, H, N, d, _stream_handle(stream, q.device))
     _check(st, "attn_fp8_prepare")
     return (*codes, *scales)
 
@@ -298,10 +311,11 @@ def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False,
 
 
 def attn_fwd_fp8_pipeline(q, k, v, signs=None, causal: bool = False, scale: float | None = None,
-                          per_tensor: bool = False, stream=None):
+                          per_tensor: bool = False, stream=None, rope=None, rope_interleaved: bool = False):
     """fp8_prepare followed by attn_fwd_fp8 (the quantised operands are
     allocated here, as torch tensors)."""
-    q8, k8, v8, qs, ks, vs = fp8_prepare(q, k, v, signs=signs, per_tensor=per_tensor, stream=stream)
+    q8, k8, v8, qs, ks, vs = fp8_prepare(q, k, v, signs=signs, per_tensor=per_tensor, stream=stream,
+                                         rope=rope, rope_interleaved=rope_interleaved)
     return attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=causal, scale=scale, stream=stream)
 
 

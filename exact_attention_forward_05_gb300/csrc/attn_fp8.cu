@@ -10,6 +10,12 @@
 // unchanged; V is not rotated.  A per-tensor mode (one scale per tensor, no
 // rotation) gives the naive FP8 baseline the pages compare against.
 //
+// The same section names rotary embeddings as the memory-bound step the
+// Hadamard transform is fused into: given cos / sin tables, the pre-pass first
+// applies the rotary embedding to Q and K (RoFormer's pairwise rotation, pairs
+// (2i, 2i+1) or (i, i + d/2)), in the registers that then take the rotation,
+// so the fused step reads and writes each row once.
+//
 // The attention kernel itself is attn_kernel::attn_fwd_kernel<128, E4M3>.
 #include "attn_kernel.cuh"
 
@@ -30,6 +36,9 @@ struct PrepParams {
   uint8_t* dst[3];
   float* scale[3];
   const int8_t* signs;  // [H][128] +-1, or nullptr (no rotation)
+  const float* rcos;    // [N][64] rotary tables, or nullptr (no rotary embedding)
+  const float* rsin;
+  int rope_interleaved; // pairs (2i, 2i+1) if nonzero, else (i, i + 64)
   int H, N, nblk;
 };
 
@@ -106,6 +115,49 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const PrepPar
   } else {
 #pragma unroll
     for (int e = 0; e < 32; ++e) x[e] = 0.f;
+  }
+  if (t < 2 && p.rcos != nullptr) {
+    // Rotary embedding: (a, b) -> (a cos - b sin, a sin + b cos).  Block-uniform
+    // branch (the half-split form shuffles); rows past N are zero and skip the
+    // table loads.
+    const bool have = row < p.N;
+    const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float* cr = p.rcos + static_cast<size_t>(have ? row : 0) * (kHeadDim / 2);
+    const float* sr = p.rsin + static_cast<size_t>(have ? row : 0) * (kHeadDim / 2);
+    if (p.rope_interleaved) {
+      // This lane's elements 32 g .. 32 g + 31 are the pairs i = 16 g .. 16 g + 15.
+      const float4* c4 = reinterpret_cast<const float4*>(cr + 16 * g);
+      const float4* s4 = reinterpret_cast<const float4*>(sr + 16 * g);
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float4 cv = have ? c4[w] : zero4, sv = have ? s4[w] : zero4;
+        const float cc[4] = {cv.x, cv.y, cv.z, cv.w}, ss[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = 8 * w + 2 * u;
+          const float a = x[e], b = x[e + 1];
+          x[e] = fmaf(a, cc[u], -b * ss[u]);
+          x[e + 1] = fmaf(a, ss[u], b * cc[u]);
+        }
+      }
+    } else {
+      // Pair i = 32 (g & 1) + e is (element i, element i + 64): lanes g and g ^ 2
+      // of the row's group hold its two halves.
+      const float4* c4 = reinterpret_cast<const float4*>(cr + 32 * (g & 1));
+      const float4* s4 = reinterpret_cast<const float4*>(sr + 32 * (g & 1));
+      const float sgn = (g & 2) ? 1.f : -1.f;  // second half: b cos + a sin
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const float4 cv = have ? c4[w] : zero4, sv = have ? s4[w] : zero4;
+        const float cc[4] = {cv.x, cv.y, cv.z, cv.w}, ss[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = 4 * w + u;
+          const float o = __shfl_xor_sync(0xffffffffu, x[e], 2);
+          x[e] = fmaf(o, sgn * ss[u], x[e] * cc[u]);
+        }
+      }
+    }
   }
   if (rotate) {
     // Signs (+1 = 0x01, -1 = 0xff): bit 7 of each byte becomes the float's sign bit.
@@ -212,13 +264,16 @@ namespace attn_internal {
 cudaError_t fp8_status_exchange(unsigned int* out) { return attn_kernel::status_exchange(out); }
 }  // namespace attn_internal
 
-ATTN_EXPORT attn_status attn_fp8_prepare(const void* q, const void* k, const void* v, attn_dtype in_dtype,
-                                         void* q8, void* k8, void* v8, float* q_scale, float* k_scale,
-                                         float* v_scale, const int8_t* signs, int per_tensor, int B,
-                                         int H, int N, int d, void* stream) {
+ATTN_EXPORT attn_status attn_fp8_prepare_rotary(const void* q, const void* k, const void* v,
+                                                attn_dtype in_dtype, void* q8, void* k8, void* v8,
+                                                float* q_scale, float* k_scale, float* v_scale,
+                                                const int8_t* signs, int per_tensor, const float* rope_cos,
+                                                const float* rope_sin, int rope_interleaved, int B, int H,
+                                                int N, int d, void* stream) {
   attn_status st = check_common(B, H, N, d);
   if (st != ATTN_OK) return st;
   if (in_dtype != ATTN_FP16 && in_dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if ((rope_cos == nullptr) != (rope_sin == nullptr)) return ATTN_ERR_INVALID_ARG;
   if (static_cast<int64_t>(B) * H * N == 0) return ATTN_OK;
   if (!q || !k || !v || !q8 || !k8 || !v8 || !q_scale || !k_scale || !v_scale) return ATTN_ERR_INVALID_ARG;
   using attn_internal::aligned;
@@ -227,6 +282,7 @@ ATTN_EXPORT attn_status attn_fp8_prepare(const void* q, const void* k, const voi
     return ATTN_ERR_MISALIGNED;
   if (!aligned(q_scale, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4)) return ATTN_ERR_MISALIGNED;
   if (signs && !aligned(signs, 16)) return ATTN_ERR_MISALIGNED;  // read 16 signs per load
+  if (rope_cos && (!aligned(rope_cos, 16) || !aligned(rope_sin, 16))) return ATTN_ERR_MISALIGNED;
   PrepParams prm;
   prm.src[0] = q; prm.src[1] = k; prm.src[2] = v;
   prm.dst[0] = static_cast<uint8_t*>(q8);
@@ -234,6 +290,9 @@ ATTN_EXPORT attn_status attn_fp8_prepare(const void* q, const void* k, const voi
   prm.dst[2] = static_cast<uint8_t*>(v8);
   prm.scale[0] = q_scale; prm.scale[1] = k_scale; prm.scale[2] = v_scale;
   prm.signs = signs;
+  prm.rcos = rope_cos;
+  prm.rsin = rope_sin;
+  prm.rope_interleaved = rope_interleaved ? 1 : 0;
   prm.H = H;
   prm.N = N;
   prm.nblk = (N + kQuantRows - 1) / kQuantRows;
@@ -241,6 +300,14 @@ ATTN_EXPORT attn_status attn_fp8_prepare(const void* q, const void* k, const voi
   const int BH = B * H;
   return in_dtype == ATTN_BF16 ? run_prepare<true>(prm, BH, per_tensor, s)
                                : run_prepare<false>(prm, BH, per_tensor, s);
+}
+
+ATTN_EXPORT attn_status attn_fp8_prepare(const void* q, const void* k, const void* v, attn_dtype in_dtype,
+                                         void* q8, void* k8, void* v8, float* q_scale, float* k_scale,
+                                         float* v_scale, const int8_t* signs, int per_tensor, int B,
+                                         int H, int N, int d, void* stream) {
+  return attn_fp8_prepare_rotary(q, k, v, in_dtype, q8, k8, v8, q_scale, k_scale, v_scale, signs,
+                                 per_tensor, nullptr, nullptr, 0, B, H, N, d, stream);
 }
 
 ATTN_EXPORT attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale,

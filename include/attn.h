@@ -195,6 +195,31 @@ attn_status attn_fp8_prepare(const void* q, const void* k, const void* v, attn_d
                              int N, int d, void* stream);
 
 /*
+ * attn_fp8_prepare_rotary -- attn_fp8_prepare with the rotary position
+ * embedding of Q and K fused in front of the rotation ("Incoherent Processing
+ * for FP8 Accuracy", FlashAttention-3 podcast page: the Hadamard transform is
+ * fused into the memory-bound rotary step).  The pages do not define the
+ * embedding; it is RoFormer's: pair i of the row at position n, a feature pair
+ * (a, b), becomes (a cos - b sin, a sin + b cos) with cos, sin the table
+ * entries (n, i).
+ *
+ *   rope_cos, rope_sin : [N, d/2] device float32, row n for query / key row n
+ *                        (the caller's rotary cache, position offset and
+ *                        frequencies included), 16-byte aligned (else
+ *                        ATTN_ERR_MISALIGNED); both NULL = no embedding, exactly
+ *                        attn_fp8_prepare; one NULL = ATTN_ERR_INVALID_ARG.
+ *   rope_interleaved   : nonzero = pairs (2i, 2i+1), 0 = pairs (i, i + d/2).
+ * Order per row of Q and K: rotary embedding, sign flip, Hadamard transform,
+ * quantisation, all in float32 registers in one pass.  V is untouched by
+ * both rotations.  Other arguments, rules and errors: attn_fp8_prepare.
+ */
+attn_status attn_fp8_prepare_rotary(const void* q, const void* k, const void* v, attn_dtype in_dtype,
+                                    void* q8, void* k8, void* v8, float* q_scale, float* k_scale,
+                                    float* v_scale, const int8_t* signs, int per_tensor,
+                                    const float* rope_cos, const float* rope_sin, int rope_interleaved,
+                                    int B, int H, int N, int d, void* stream);
+
+/*
  * attn_fwd_fp8 -- exact attention forward on E4M3 operands with float32 scales
  * (as written by attn_fp8_prepare), bf16 output.
  *

@@ -165,3 +165,22 @@ def test_fp8_validation_before_launch(lib):
     assert fwd(o=None) == attn.ATTN_ERR_INVALID_ARG
     assert fwd(v8=0x6001) == attn.ATTN_ERR_MISALIGNED
     assert fwd(N=0) == attn.ATTN_OK
+
+
+def test_fp8_rotary_validation_before_launch(lib):
+    args = dict(q=0x1000, k=0x2000, v=0x3000, q8=0x4000, k8=0x5000, v8=0x6000, qs=0x7000,
+                ks=0x8000, vs=0x9000, cos=0xC000, sin=0xD000)
+
+    def prep(d=128, N=64, **kw):
+        a = dict(args, **kw)
+        return lib.attn_fp8_prepare_rotary(a["q"], a["k"], a["v"], attn.ATTN_BF16, a["q8"], a["k8"],
+                                           a["v8"], a["qs"], a["ks"], a["vs"], None, 0, a["cos"],
+                                           a["sin"], 0, 1, 2, N, d, None)
+
+    assert prep(cos=None) == attn.ATTN_ERR_INVALID_ARG  # one table without the other
+    assert prep(sin=None) == attn.ATTN_ERR_INVALID_ARG
+    assert prep(cos=None, sin=None, N=0) == attn.ATTN_OK
+    assert prep(cos=0xC004) == attn.ATTN_ERR_MISALIGNED
+    assert prep(sin=0xD008) == attn.ATTN_ERR_MISALIGNED
+    assert prep(d=64) == attn.ATTN_ERR_UNSUPPORTED
+    assert prep(N=0) == attn.ATTN_OK

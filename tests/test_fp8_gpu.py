@@ -175,3 +175,67 @@ def test_fp8_empty_and_bad_arguments():
     with pytest.raises(attn.AttnError) as e:
         attn.fp8_prepare(q, q, q)
     assert e.value.status == attn.ATTN_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("interleaved", [False, True])
+@pytest.mark.parametrize("rotate", [False, True])
+def test_prepare_with_rotary_matches_oracle(interleaved, rotate):
+    """Rotary embedding fused in front of the rotation: Q and K against the
+    oracle's rotary -> rotation -> block quantisation (float32 on the device,
+    float64 in the oracle: scales to float32 rounding, dequantised values within
+    one E4M3 step, few codes different); V untouched, bit-exact.  N = 385 leaves
+    a ragged last block (rows past N skip the table loads)."""
+    B, H, N = 2, 3, 385
+    q, k, v = synth.outlier_inputs(B, H, N, D, "bf16", seed=7)
+    signs = synth.hadamard_signs(H, D, seed=7) if rotate else None
+    cos, sin = synth.rotary_tables(N, D, offset=5)
+    out = attn.fp8_prepare(q.cuda(), k.cuda(), v.cuda(), signs=None if signs is None else signs.cuda(),
+                           rope=(cos.cuda(), sin.cuda()), rope_interleaved=interleaved)
+    torch.cuda.synchronize()
+    for i, x in enumerate((q, k)):
+        ref = oracle.rotary(x, cos, sin, interleaved)
+        if rotate:
+            ref = oracle.hadamard_rotate(ref, signs)
+        codes, scales = oracle.block_quantize(ref)
+        np.testing.assert_allclose(_np(out[3 + i]), scales, rtol=1e-5, atol=0)
+        deq_gpu = oracle.dequantize(_np(out[i]), _np(out[3 + i]))
+        deq_ref = oracle.dequantize(codes, scales)
+        s_rep = np.repeat(scales.astype(np.float64), 128, axis=-1)[..., :N, None]
+        assert np.all(np.abs(deq_gpu - deq_ref) <= _e4m3_step(deq_ref / s_rep) * s_rep * (1 + 1e-6))
+        assert np.mean(_np(out[i]) != codes) < 0.01
+    codes, scales = oracle.block_quantize(v)
+    np.testing.assert_array_equal(_np(out[2]), codes)
+    np.testing.assert_array_equal(_np(out[5]), scales)
+
+
+def test_prepare_without_tables_is_unchanged():
+    """No tables: the rotary entry point is the plain pre-pass, bit for bit."""
+    q, k, v = (t.cuda() for t in synth.outlier_inputs(1, 2, 300, D, "bf16", seed=8))
+    signs = synth.hadamard_signs(2, D, seed=8).cuda()
+    a = attn.fp8_prepare(q, k, v, signs=signs)
+    b = attn.fp8_prepare(q, k, v, signs=signs, rope=None)
+    cos, sin = (torch.zeros(300, 64, device="cuda") for _ in range(2))
+    cos += 1.0  # zero angles: the embedding is the identity, exactly
+    c = attn.fp8_prepare(q, k, v, signs=signs, rope=(cos, sin))
+    torch.cuda.synchronize()
+    for x, y, z in zip(a, b, c):
+        assert torch.equal(x, y) and torch.equal(x, z)
+
+
+@pytest.mark.parametrize("interleaved", [False, True])
+def test_fp8_pipeline_with_rotary_against_exact_attention(interleaved):
+    """End to end: FP8 pipeline with the fused rotary embedding against exact
+    attention on the rotary-embedded 16-bit inputs (sampled rows), within the
+    FP8 bound."""
+    B, H, N = 1, 4, 2048
+    q, k, v = synth.outlier_inputs(B, H, N, D, "bf16", seed=9)
+    signs = synth.hadamard_signs(H, D, seed=9)
+    cos, sin = synth.rotary_tables(N, D)
+    o, _ = attn.attn_fwd_fp8_pipeline(q.cuda(), k.cuda(), v.cuda(), signs=signs.cuda(),
+                                      rope=(cos.cuda(), sin.cuda()), rope_interleaved=interleaved)
+    torch.cuda.synchronize()
+    rows = synth.sample_rows(N, 32, seed=9)
+    qr, kr = oracle.rotary(q, cos, sin, interleaved), oracle.rotary(k, cos, sin, interleaved)
+    o_ref, _ = oracle.attention(qr, kr, v, scale=D ** -0.5, rows=rows)
+    err = _np(o.float())[:, :, rows] - o_ref
+    assert math.sqrt(np.mean(err ** 2)) <= FP8_RMS
