@@ -21,6 +21,8 @@
 
 using attn_kernel::FwdParams;
 using attn_kernel::KIND_E4M3;
+using sm103::fadd2;
+using sm103::ffma2;
 
 namespace {
 
@@ -42,27 +44,56 @@ struct PrepParams {
   int H, N, nblk;
 };
 
+// Paired float32 arithmetic (one instruction for two lanes of a register pair,
+// each rounded as the scalar operation would be).
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(*reinterpret_cast<unsigned long long*>(&a)),
+      "l"(*reinterpret_cast<unsigned long long*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(*reinterpret_cast<unsigned long long*>(&a)),
+      "l"(*reinterpret_cast<unsigned long long*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float2 pair(const float (&x)[32], int e) { return make_float2(x[e], x[e + 1]); }
+__device__ __forceinline__ void put(float (&x)[32], int e, float2 v) {
+  x[e] = v.x;
+  x[e + 1] = v.y;
+}
+
 // Sylvester-ordered fast Walsh-Hadamard transform of one 128-element row held
 // by 4 lanes (lane g of the group owns elements 32 g .. 32 g + 31): butterflies
 // of stride 1 .. 16 inside the thread, 32 and 64 across the group.  The stages
-// commute, so any order gives the transform.
+// commute, so any order gives the transform.  Strides 2 .. 16 and the lane
+// stages combine whole element pairs with paired instructions.
 __device__ __forceinline__ void fwht128(float (&x)[32], int g) {
 #pragma unroll
-  for (int m = 1; m < 32; m <<= 1)
+  for (int e = 0; e < 32; e += 2) {
+    const float a = x[e], b = x[e + 1];
+    x[e] = a + b;
+    x[e + 1] = a - b;
+  }
 #pragma unroll
-    for (int e = 0; e < 32; ++e)
+  for (int m = 2; m < 32; m <<= 1)
+#pragma unroll
+    for (int e = 0; e < 32; e += 2)
       if ((e & m) == 0) {
-        const float a = x[e], b = x[e + m];
-        x[e] = a + b;
-        x[e + m] = a - b;
+        const float2 a = pair(x, e), b = pair(x, e + m);
+        put(x, e, fadd2(a, b));
+        put(x, e + m, fsub2(a, b));
       }
 #pragma unroll
   for (int m = 1; m < 4; m <<= 1) {
     const float sgn = (g & m) ? -1.f : 1.f;  // upper half of the pair: partner - own
+    const float2 sg2 = make_float2(sgn, sgn);
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const float o = __shfl_xor_sync(0xffffffffu, x[e], m);
-      x[e] = fmaf(x[e], sgn, o);
+    for (int e = 0; e < 32; e += 2) {
+      const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, x[e], m),
+                                   __shfl_xor_sync(0xffffffffu, x[e + 1], m));
+      put(x, e, ffma2(pair(x, e), sg2, o));
     }
   }
 }
@@ -72,11 +103,11 @@ __device__ __forceinline__ void fwht128(float (&x)[32], int g) {
 // System/6000 processor", IBM J. Res. Dev. 34(1), 1990): q0 = RN(x y),
 // r = x - s q0 exactly, q = RN(q0 + r y).  Used where |x / s| <= 448 and s is
 // a normal number far from the exponent limits; other scales take the
-// division itself.
-__device__ __forceinline__ float div_by_scale(float x, float s, float y) {
-  const float q0 = x * y;
-  const float r = fmaf(-q0, s, x);
-  return fmaf(r, y, q0);
+// division itself.  Two quotients at a time: ns2 = (-s, -s), y2 = (y, y).
+__device__ __forceinline__ float2 div_by_scale2(float2 x, float2 ns2, float2 y2) {
+  const float2 q0 = fmul2(x, y2);
+  const float2 r = ffma2(q0, ns2, x);
+  return ffma2(r, y2, q0);
 }
 
 template <bool BF16IN, int MODE>
@@ -136,8 +167,9 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const PrepPar
         for (int u = 0; u < 4; ++u) {
           const int e = 8 * w + 2 * u;
           const float a = x[e], b = x[e + 1];
-          x[e] = fmaf(a, cc[u], -b * ss[u]);
-          x[e + 1] = fmaf(a, ss[u], b * cc[u]);
+          // (a c - b s, a s + b c): b (-s, c), then a (c, s) added with one rounding.
+          const float2 t2 = fmul2(make_float2(b, b), make_float2(-ss[u], cc[u]));
+          put(x, e, ffma2(make_float2(a, a), make_float2(cc[u], ss[u]), t2));
         }
       }
     } else {
@@ -151,10 +183,12 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const PrepPar
         const float4 cv = have ? c4[w] : zero4, sv = have ? s4[w] : zero4;
         const float cc[4] = {cv.x, cv.y, cv.z, cv.w}, ss[4] = {sv.x, sv.y, sv.z, sv.w};
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 4; u += 2) {
           const int e = 4 * w + u;
-          const float o = __shfl_xor_sync(0xffffffffu, x[e], 2);
-          x[e] = fmaf(o, sgn * ss[u], x[e] * cc[u]);
+          const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, x[e], 2),
+                                       __shfl_xor_sync(0xffffffffu, x[e + 1], 2));
+          const float2 t2 = fmul2(pair(x, e), make_float2(cc[u], cc[u + 1]));
+          put(x, e, ffma2(o, make_float2(sgn * ss[u], sgn * ss[u + 1]), t2));
         }
       }
     }
@@ -173,9 +207,9 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const PrepPar
       x[e] = __uint_as_float(__float_as_uint(x[e]) ^ bit);
     }
     fwht128(x, g);
-    const float inv_sqrt_d = 0.08838834764831845f;  // 1 / sqrt(128)
+    const float2 inv_sqrt_d = make_float2(0.08838834764831845f, 0.08838834764831845f);  // 1 / sqrt(128)
 #pragma unroll
-    for (int e = 0; e < 32; ++e) x[e] *= inv_sqrt_d;
+    for (int e = 0; e < 32; e += 2) put(x, e, fmul2(pair(x, e), inv_sqrt_d));
   }
 
   // amax of the block
@@ -208,14 +242,19 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const PrepPar
     const float y = __frcp_rn(s);
     if (row < p.N) {
       uint32_t pk[8];
+      const float2 ns2 = make_float2(-s, -s), y2 = make_float2(y, y);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        float q[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          q[e] = fast ? div_by_scale(x[4 * k + e], s, y) : __fdiv_rn(x[4 * k + e], s);
-        const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(q[0], q[1]), __NV_SATFINITE, __NV_E4M3);
-        const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(q[2], q[3]), __NV_SATFINITE, __NV_E4M3);
+        float2 q01, q23;
+        if (fast) {
+          q01 = div_by_scale2(pair(x, 4 * k), ns2, y2);
+          q23 = div_by_scale2(pair(x, 4 * k + 2), ns2, y2);
+        } else {
+          q01 = make_float2(__fdiv_rn(x[4 * k], s), __fdiv_rn(x[4 * k + 1], s));
+          q23 = make_float2(__fdiv_rn(x[4 * k + 2], s), __fdiv_rn(x[4 * k + 3], s));
+        }
+        const uint32_t lo = __nv_cvt_float2_to_fp8x2(q01, __NV_SATFINITE, __NV_E4M3);
+        const uint32_t hi = __nv_cvt_float2_to_fp8x2(q23, __NV_SATFINITE, __NV_E4M3);
         pk[k] = lo | (hi << 16);
       }
       uint4* out = reinterpret_cast<uint4*>(dst + head + static_cast<size_t>(row) * kHeadDim + 32 * g);
