@@ -16,6 +16,9 @@ Definitions (each cited where it is computed, in ``oracle.c``):
 * ``hadamard_rotate``: x -> (x * sigma) H_d / sqrt(d) with the Sylvester
   Hadamard matrix, the random-sign rotation of "Incoherent Processing for FP8
   Accuracy" (FlashAttention-3 podcast page).
+* ``attention_bwd``: dQ, dK, dV of ``attention`` for a given dL/dO, the chain
+  rule through the definition (the pages name the backward pass and its
+  recomputation, "FlashAttention v1.", but print no gradient formulas).
 * ``rotary``: the rotary position embedding that the same section names as the
   memory-bound step the rotation is fused into; the pages do not define it, so
   it is RoFormer's pairwise rotation by position-dependent angles, with the
@@ -80,6 +83,9 @@ def _load():
             lib.oracle_hadamard_entry.restype = i32
             lib.oracle_hadamard_rotate.argtypes = [dp, dp, dp, i64, i64, i64, i64]
             lib.oracle_hadamard_rotate.restype = i32
+            lib.oracle_attention_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, i64, i64, i64, i64, i32,
+                                                 ctypes.c_double, i32]
+            lib.oracle_attention_bwd.restype = i32
             lib.oracle_rotary.argtypes = [dp, dp, dp, dp, i64, i64, i64, i32]
             lib.oracle_rotary.restype = i32
             lib.oracle_block_quantize.argtypes = [dp, dp, dp, i64, i64, i64, i64, i32]
@@ -162,6 +168,26 @@ def hadamard_rotate(x, signs) -> np.ndarray:
     if st != 0:
         raise ValueError("hadamard_rotate: d must be a power of two")
     return out
+
+
+def attention_bwd(q, k, v, dout, causal=False, scale: float | None = None, nthreads: int = 0):
+    """Gradients (dQ, dK, dV) of ``attention`` for dL/dO = ``dout``, float64.
+
+    q, dout: [B, H, Nq, d]; k, v: [B, H, Nk, d]; ``causal`` as for
+    ``attention``.  lse is an auxiliary output: no gradient flows through it.
+    """
+    q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, H, N, d = q.shape
+    if k.shape != v.shape or k.shape[:2] != (B, H) or k.shape[3] != d or g.shape != q.shape:
+        raise ValueError("k, v must be [B, H, Nk, d] and dout like q")
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    st = _load().oracle_attention_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(dq), _ptr(dk), _ptr(dv),
+                                      B * H, N, k.shape[2], d, int(causal), float(scale), int(nthreads))
+    if st != 0:
+        raise RuntimeError(f"oracle_attention_bwd failed with status {st}")
+    return dq, dk, dv
 
 
 def rotary(x, cos, sin, interleaved: bool = False) -> np.ndarray:

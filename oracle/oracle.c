@@ -54,6 +54,13 @@ typedef struct {
     int status;
 } att_job;
 
+/* Keys 0 .. visible_keys(...) - 1 are the ones query row i sees. */
+static int64_t visible_keys(int64_t i, int64_t Nq, int64_t Nk, int causal) {
+    if (causal == 1) return i + 1 < Nk ? i + 1 : Nk;
+    if (causal == 2) return i + 1 + (Nk - Nq);
+    return Nk;
+}
+
 static void *att_worker(void *arg) {
     att_job *J = (att_job *)arg;
     double *w = (double *)malloc(sizeof(double) * (size_t)(J->Nk > 0 ? J->Nk : 1));
@@ -65,9 +72,7 @@ static void *att_worker(void *arg) {
         const double *qi = J->q + (bh * J->Nq + i) * J->d;
         const double *kh = J->k + bh * J->Nk * J->d;
         const double *vh = J->v + bh * J->Nk * J->d;
-        int64_t nkeys = J->Nk;                               /* keys 0..nkeys-1 */
-        if (J->causal == 1 && i + 1 < nkeys) nkeys = i + 1;
-        if (J->causal == 2) nkeys = i + 1 + (J->Nk - J->Nq);
+        const int64_t nkeys = visible_keys(i, J->Nq, J->Nk, J->causal);
         double m = -INFINITY;
         for (int64_t j = 0; j < nkeys; ++j) {
             double dot = 0.0;
@@ -137,6 +142,116 @@ ORACLE_API int oracle_attention(const double *q, const double *k, const double *
                                 int nthreads, int *threads_used) {
     return oracle_attention_qk(q, k, v, o, lse, BH, N, N, d, causal ? 1 : 0, scale, rows, nrows,
                                nthreads, threads_used);
+}
+
+/* ----------------------------------------------------------- backward */
+
+/* Gradients of the attention above with respect to Q, K and V, given
+ * dout = dL/dO for a scalar loss L (lse is treated as an auxiliary output:
+ * no gradient flows through it).  The pages only say that the fused kernels
+ * recompute the forward intermediates in the backward pass ("FlashAttention --
+ * one, two, three!", section "FlashAttention v1."); the gradients themselves
+ * are the chain rule through the definition, row by row:
+ *
+ *   p_ij  = softmax over the visible keys j of s_ij = scale q_i . k_j
+ *   dv_j += p_ij g_i                                  (g_i = dout row i)
+ *   dp_ij = g_i . v_j
+ *   ds_ij = p_ij (dp_ij - sum_l p_il dp_il)          (softmax Jacobian)
+ *   dq_i  = scale sum_j ds_ij k_j
+ *   dk_j += scale ds_ij q_i
+ *
+ * Heads are spread over POSIX threads (each head's dk, dv are its own). */
+typedef struct {
+    const double *q, *k, *v, *g;
+    double *dq, *dk, *dv;
+    int64_t BH, Nq, Nk, d;
+    int causal;
+    double scale;
+    int tid, nthreads;
+    int status;
+} bwd_job;
+
+static void *bwd_worker(void *arg) {
+    bwd_job *J = (bwd_job *)arg;
+    double *p = (double *)malloc(sizeof(double) * (size_t)J->Nk);
+    double *dp = (double *)malloc(sizeof(double) * (size_t)J->Nk);
+    if (!p || !dp) { free(p); free(dp); J->status = 1; return NULL; }
+    for (int64_t bh = J->tid; bh < J->BH; bh += J->nthreads) {
+        const int64_t qoff = bh * J->Nq * J->d, koff = bh * J->Nk * J->d;
+        const double *qh = J->q + qoff, *gh = J->g + qoff, *kh = J->k + koff, *vh = J->v + koff;
+        double *dqh = J->dq + qoff, *dkh = J->dk + koff, *dvh = J->dv + koff;
+        for (int64_t x = 0; x < J->Nk * J->d; ++x) { dkh[x] = 0.0; dvh[x] = 0.0; }
+        for (int64_t i = 0; i < J->Nq; ++i) {
+            const double *qi = qh + i * J->d, *gi = gh + i * J->d;
+            const int64_t nkeys = visible_keys(i, J->Nq, J->Nk, J->causal);
+            double m = -INFINITY;
+            for (int64_t j = 0; j < nkeys; ++j) {
+                const double *kj = kh + j * J->d;
+                double sij = 0.0;
+                for (int64_t c = 0; c < J->d; ++c) sij += qi[c] * kj[c];
+                p[j] = J->scale * sij;
+                if (p[j] > m) m = p[j];
+            }
+            double l = 0.0;
+            for (int64_t j = 0; j < nkeys; ++j) {
+                p[j] = exp(p[j] - m);
+                l += p[j];
+            }
+            double rowdot = 0.0;                             /* sum_l p_il dp_il */
+            for (int64_t j = 0; j < nkeys; ++j) {
+                p[j] /= l;
+                double dot = 0.0;
+                for (int64_t c = 0; c < J->d; ++c) dot += gi[c] * vh[j * J->d + c];
+                dp[j] = dot;
+                rowdot += p[j] * dp[j];
+            }
+            double *dqi = dqh + i * J->d;
+            for (int64_t c = 0; c < J->d; ++c) dqi[c] = 0.0;
+            for (int64_t j = 0; j < nkeys; ++j) {
+                const double ds = p[j] * (dp[j] - rowdot);
+                for (int64_t c = 0; c < J->d; ++c) {
+                    dqi[c] += J->scale * ds * kh[j * J->d + c];
+                    dkh[j * J->d + c] += J->scale * ds * qi[c];
+                    dvh[j * J->d + c] += p[j] * gi[c];
+                }
+            }
+        }
+    }
+    free(p);
+    free(dp);
+    return NULL;
+}
+
+/* q, dout, dq: [BH, Nq, d]; k, v, dk, dv: [BH, Nk, d]; float64.  causal as for
+ * oracle_attention_qk (rows without a visible key are rejected).  Returns 0
+ * on success (2: bad arguments). */
+ORACLE_API int oracle_attention_bwd(const double *q, const double *k, const double *v,
+                                    const double *dout, double *dq, double *dk, double *dv,
+                                    int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int causal,
+                                    double scale, int nthreads) {
+    if (!q || !k || !v || !dout || !dq || !dk || !dv || BH < 0 || Nq < 0 || Nk < 0 || d < 1) return 2;
+    if (causal < 0 || causal > 2) return 2;
+    if (Nq > 0 && (Nk == 0 || (causal == 2 && Nq > Nk))) return 2;
+    if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+    if (nthreads < 1) nthreads = 1;
+    if (BH < nthreads) nthreads = (int)(BH > 0 ? BH : 1);
+    bwd_job *jobs = (bwd_job *)calloc((size_t)nthreads, sizeof(bwd_job));
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !th) { free(jobs); free(th); return 1; }
+    for (int t = 0; t < nthreads; ++t) {
+        bwd_job J = {q, k, v, dout, dq, dk, dv, BH, Nq, Nk, d, causal, scale, t, nthreads, 0};
+        jobs[t] = J;
+    }
+    for (int t = 1; t < nthreads; ++t)
+        if (pthread_create(&th[t], NULL, bwd_worker, &jobs[t]) != 0) { jobs[t].status = 1; th[t] = 0; }
+    bwd_worker(&jobs[0]);
+    int st = 0;
+    for (int t = 1; t < nthreads; ++t)
+        if (th[t]) pthread_join(th[t], NULL);
+    for (int t = 0; t < nthreads; ++t) st |= jobs[t].status;
+    free(jobs);
+    free(th);
+    return st;
 }
 
 /* ------------------------------------------------------------ E4M3 codec */

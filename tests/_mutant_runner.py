@@ -34,6 +34,48 @@ def main_rotary(lib_path):
     return 0
 
 
+def _attn_and_bwd(lib):
+    i64, dp, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+    fn = lib.oracle_attention_qk
+    fn.argtypes = [dp, dp, dp, dp, dp, i64, i64, i64, i64, i32, ctypes.c_double, dp, i64, i32, dp]
+    fn.restype = i32
+    bw = lib.oracle_attention_bwd
+    bw.argtypes = [dp, dp, dp, dp, dp, dp, dp, i64, i64, i64, i64, i32, ctypes.c_double, i32]
+    bw.restype = i32
+    p = lambda a: ctypes.c_void_p(a.ctypes.data)
+
+    def attn(q, k, v, causal, scale):
+        q, k, v = (np.ascontiguousarray(a, dtype=np.float64) for a in (q, k, v))
+        B, H, N, d = q.shape
+        o, lse = np.empty((B, H, N, d)), np.empty((B, H, N))
+        assert fn(p(q), p(k), p(v), p(o), p(lse), B * H, N, k.shape[2], d, int(causal), float(scale),
+                  None, N, 1, None) == 0
+        return o, lse
+
+    def bwd(q, k, v, g, causal, scale):
+        q, k, v, g = (np.ascontiguousarray(a, dtype=np.float64) for a in (q, k, v, g))
+        B, H, N, d = q.shape
+        dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+        assert bw(p(q), p(k), p(v), p(g), p(dq), p(dk), p(dv), B * H, N, k.shape[2], d, int(causal),
+                  float(scale), 1) == 0
+        return dq, dk, dv
+
+    return attn, bwd
+
+
+def main_bwd(lib_path):
+    attn, bwd = _attn_and_bwd(ctypes.CDLL(lib_path))
+    failed = []
+    for check in pins.BWD_CHECKS:
+        try:
+            with np.errstate(all="ignore"):
+                check(attn, bwd)
+        except AssertionError:
+            failed.append(check.__name__)
+    print("failed:", ",".join(failed))
+    return 1 if failed else 0
+
+
 def main(lib_path):
     lib = ctypes.CDLL(lib_path)
     i64, dp, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
@@ -67,4 +109,5 @@ def main(lib_path):
 
 
 if __name__ == "__main__":
-    sys.exit(main_rotary(sys.argv[1]) if sys.argv[2:] == ["rotary"] else main(sys.argv[1]))
+    mode = sys.argv[2] if len(sys.argv) > 2 else ""
+    sys.exit({"rotary": main_rotary, "bwd": main_bwd}.get(mode, main)(sys.argv[1]))

@@ -287,3 +287,86 @@ ALL_CHECKS = [check_zero_query_is_mean, check_zero_scale_is_mean, check_causal_r
               check_logit_shift, check_orthogonal_invariance, check_brute_force,
               check_golden, check_row_subset, check_brute_force_cross, check_cross_zero_query,
               check_end_aligned_is_suffix_of_self_attention]
+
+
+# ------------------------------------------------------------------ backward
+# Each check takes ``attn`` as above and ``bwd(q, k, v, g, causal, scale) ->
+# (dQ, dK, dV)``, the gradients for dL/dO = g.
+
+def _loss(attn, q, k, v, g, causal, scale):
+    o, _ = attn(q, k, v, causal, scale)
+    return float(np.sum(o * g))
+
+
+def check_bwd_finite_differences(attn, bwd):
+    """Every entry of dQ, dK, dV against central differences of L = sum(G * O)
+    through the forward oracle (step 1e-5: truncation ~1e-10, rounding
+    ~1e-11), for no mask and both causal alignments, Nq != Nk."""
+    eps = 1e-5
+    for (B, H, Nq, Nk, d), causal, seed in (((1, 2, 4, 6, 3), 0, 90), ((1, 1, 5, 5, 2), 1, 91),
+                                            ((1, 1, 3, 6, 3), 2, 92), ((1, 1, 6, 4, 2), 1, 93)):
+        q = _rand((B, H, Nq, d), seed)
+        k, v = _rand((B, H, Nk, d), seed + 1), _rand((B, H, Nk, d), seed + 2)
+        g = _rand((B, H, Nq, d), seed + 3)
+        scale = 0.7
+        grads = bwd(q, k, v, g, causal, scale)
+        for which, (x, dx) in enumerate(zip((q, k, v), grads)):
+            num = np.zeros_like(x)
+            for idx in np.ndindex(*x.shape):
+                args = [q.copy(), k.copy(), v.copy()]
+                args[which][idx] += eps
+                up = _loss(attn, *args, g, causal, scale)
+                args[which][idx] -= 2 * eps
+                down = _loss(attn, *args, g, causal, scale)
+                num[idx] = (up - down) / (2 * eps)
+            np.testing.assert_allclose(dx, num, rtol=0, atol=1e-7)
+
+
+def check_bwd_sums(attn, bwd):
+    """Rows of the softmax Jacobian sum to zero, so the key gradients of a head
+    sum to zero; rows of P sum to one, so the value gradients sum to the
+    summed output gradient."""
+    B, H, Nq, Nk, d = 2, 2, 9, 13, 4
+    q = _rand((B, H, Nq, d), 94)
+    k, v = _rand((B, H, Nk, d), 95), _rand((B, H, Nk, d), 96)
+    g = _rand((B, H, Nq, d), 97)
+    for causal in (0, 1, 2):
+        _, dk, dv = bwd(q, k, v, g, causal, 0.5)
+        np.testing.assert_allclose(dk.sum(axis=2), 0.0, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dv.sum(axis=2), g.sum(axis=2), rtol=0, atol=1e-12)
+
+
+def check_bwd_zero_scale(attn, bwd):
+    """scale = 0: every logit is 0, so dQ = dK = 0 and dV_j is the sum over
+    the rows that see key j of g_i / (number of keys row i sees)."""
+    B, H, Nq, Nk, d = 1, 2, 6, 8, 3
+    q = _rand((B, H, Nq, d), 98)
+    k, v = _rand((B, H, Nk, d), 99), _rand((B, H, Nk, d), 100)
+    g = _rand((B, H, Nq, d), 101)
+    for causal in (0, 1, 2):
+        dq, dk, dv = bwd(q, k, v, g, causal, 0.0)
+        assert np.all(dq == 0) and np.all(dk == 0)
+        want = np.zeros_like(v)
+        for i in range(Nq):
+            n = visible_keys(i, Nq, Nk, causal)
+            want[:, :, :n] += g[:, :, i:i + 1] / n
+        np.testing.assert_allclose(dv, want, rtol=0, atol=1e-13)
+
+
+def check_bwd_unseen_keys_get_nothing(attn, bwd):
+    """Top-left causal mask with Nq < Nk: keys j >= Nq are seen by no row, so
+    their gradients are exactly zero; the zero output gradient gives zero
+    gradients everywhere."""
+    B, H, Nq, Nk, d = 1, 1, 4, 9, 3
+    q = _rand((B, H, Nq, d), 102)
+    k, v = _rand((B, H, Nk, d), 103), _rand((B, H, Nk, d), 104)
+    g = _rand((B, H, Nq, d), 105)
+    _, dk, dv = bwd(q, k, v, g, 1, 0.8)
+    assert np.all(dk[:, :, Nq:] == 0) and np.all(dv[:, :, Nq:] == 0)
+    assert np.any(dk[:, :, :Nq] != 0) and np.any(dv[:, :, :Nq] != 0)
+    for x in bwd(q, k, v, np.zeros_like(g), 0, 0.8):
+        assert np.all(x == 0)
+
+
+BWD_CHECKS = [check_bwd_finite_differences, check_bwd_sums, check_bwd_zero_scale,
+              check_bwd_unseen_keys_get_nothing]

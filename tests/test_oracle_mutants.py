@@ -14,9 +14,9 @@ SRC = os.path.join(ROOT, "oracle", "oracle.c")
 
 MUTANTS = [
     ("dropped scale", "w[j] = J->scale * dot;", "w[j] = dot;"),
-    ("causal mask off by one", "i + 1 < nkeys) nkeys = i + 1;", "i < nkeys) nkeys = i;"),
-    ("end-aligned mask without offset", "nkeys = i + 1 + (J->Nk - J->Nq);", "nkeys = i + 1;"),
-    ("end-aligned offset reversed", "nkeys = i + 1 + (J->Nk - J->Nq);", "nkeys = i + 1 + (J->Nq - J->Nk);"),
+    ("causal mask off by one", "return i + 1 < Nk ? i + 1 : Nk;", "return i < Nk ? i : Nk;"),
+    ("end-aligned mask without offset", "return i + 1 + (Nk - Nq);", "return i + 1;"),
+    ("end-aligned offset reversed", "return i + 1 + (Nk - Nq);", "return i + 1 + (Nq - Nk);"),
     ("value used as key", "qi[c] * kh[j * J->d + c]", "qi[c] * vh[j * J->d + c]"),
     ("sign of exponent", "w[j] = exp(w[j] - m);", "w[j] = exp(m - w[j]);"),
     ("missing normalisation", "oi[c] /= l;", "oi[c] /= 1.0;"),
@@ -38,6 +38,19 @@ ROTARY_MUTANTS = [
 ]
 
 
+# Mistakes in the backward pass, each caught by a backward pin.
+BWD_MUTANTS = [
+    ("softmax Jacobian without the row term", "const double ds = p[j] * (dp[j] - rowdot);",
+     "const double ds = p[j] * dp[j];"),
+    ("value gradient without the weights", "dvh[j * J->d + c] += p[j] * gi[c];", "dvh[j * J->d + c] += gi[c];"),
+    ("key gradient unscaled", "dkh[j * J->d + c] += J->scale * ds * qi[c];", "dkh[j * J->d + c] += ds * qi[c];"),
+    ("query gradient from values", "dqi[c] += J->scale * ds * kh[j * J->d + c];",
+     "dqi[c] += J->scale * ds * vh[j * J->d + c];"),
+    ("output gradient against keys", "dot += gi[c] * vh[j * J->d + c];", "dot += gi[c] * kh[j * J->d + c];"),
+    ("row weights not normalised", "                p[j] /= l;\n", "\n"),
+]
+
+
 def _run_mutant(tmp_path, old, new, *mode):
     src = open(SRC).read()
     assert src.count(old) == 1, f"mutation site not found once: {old!r}"
@@ -56,6 +69,12 @@ def test_mutant_fails_a_pin(tmp_path, name, old, new):
     assert res.returncode == 1, f"mutant '{name}' survived every pin: {res.stdout}{res.stderr}"
 
 
+@pytest.mark.parametrize("name,old,new", BWD_MUTANTS, ids=[m[0] for m in BWD_MUTANTS])
+def test_bwd_mutant_fails_a_pin(tmp_path, name, old, new):
+    res = _run_mutant(tmp_path, old, new, "bwd")
+    assert res.returncode == 1, f"mutant '{name}' survived every backward pin: {res.stdout}{res.stderr}"
+
+
 @pytest.mark.parametrize("name,old,new", ROTARY_MUTANTS, ids=[m[0] for m in ROTARY_MUTANTS])
 def test_rotary_mutant_fails_the_pin(tmp_path, name, old, new):
     res = _run_mutant(tmp_path, old, new, "rotary")
@@ -66,7 +85,7 @@ def test_unmutated_copy_passes_every_pin(tmp_path):
     lib = tmp_path / "libcopy.so"
     subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread", "-D_GNU_SOURCE",
                     SRC, "-o", str(lib), "-lm"], check=True)
-    for mode in ([], ["rotary"]):
+    for mode in ([], ["rotary"], ["bwd"]):
         res = subprocess.run([sys.executable, os.path.join(ROOT, "tests", "_mutant_runner.py"), str(lib), *mode],
                              capture_output=True, text=True, timeout=300)
         assert res.returncode == 0, res.stdout + res.stderr

@@ -223,3 +223,36 @@ def test_rotary_scores_depend_on_relative_position_only():
         # ... while the logits themselves do change with the relative position.
         plain = q[0, 0] @ k[0, 0].T
         assert np.abs(l0 - plain).max() > 1.0
+
+
+def _bwd(q, k, v, g, causal, scale):
+    return oracle.attention_bwd(q, k, v, g, causal=causal, scale=scale)
+
+
+@pytest.mark.parametrize("check", pins.BWD_CHECKS, ids=lambda c: c.__name__)
+def test_attention_bwd_pin(check):
+    check(_attn, _bwd)
+
+
+@pytest.mark.parametrize("causal", [0, 1, 2])
+def test_attention_bwd_matches_autograd(causal):
+    """The same gradients from PyTorch's float64 autograd through an explicit
+    masked softmax (an independent implementation of the chain rule)."""
+    B, H, Nq, Nk, d = 2, 2, 7, 11, 5
+    rng = np.random.default_rng(110 + causal)
+    q, k, v, g = (rng.standard_normal(s) for s in ((B, H, Nq, d), (B, H, Nk, d), (B, H, Nk, d), (B, H, Nq, d)))
+    qt, kt, vt = (torch.tensor(a, requires_grad=True) for a in (q, k, v))
+    s = 0.6 * qt @ kt.transpose(-1, -2)
+    i = torch.arange(Nq)[:, None]
+    j = torch.arange(Nk)[None, :]
+    limit = {0: torch.full((Nq, 1), Nk - 1), 1: i, 2: i + (Nk - Nq)}[causal]
+    s = s.masked_fill(j > limit, float("-inf"))
+    (torch.softmax(s, dim=-1) @ vt).backward(torch.tensor(g))
+    for mine, ref in zip(oracle.attention_bwd(q, k, v, g, causal=causal, scale=0.6), (qt, kt, vt)):
+        np.testing.assert_allclose(mine, ref.grad.numpy(), rtol=0, atol=1e-12)
+
+
+def test_attention_bwd_rejects_rows_without_keys():
+    q, k = np.zeros((1, 1, 4, 2)), np.zeros((1, 1, 3, 2))
+    with pytest.raises(RuntimeError):
+        oracle.attention_bwd(q, k, k, q, causal=2, scale=1.0)
