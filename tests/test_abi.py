@@ -184,3 +184,31 @@ def test_fp8_rotary_validation_before_launch(lib):
     assert prep(sin=0xD008) == attn.ATTN_ERR_MISALIGNED
     assert prep(d=64) == attn.ATTN_ERR_UNSUPPORTED
     assert prep(N=0) == attn.ATTN_OK
+
+
+def test_shape_decoding_per_layout():
+    """The binding reads (B, H, Nq, Nk, d) from q and k in either layout."""
+    import torch
+    from exact_attention_forward_05_gb300 import _qkv_shapes
+    q = torch.zeros(2, 3, 5, 64, dtype=torch.bfloat16)   # [B, H, Nq, d]
+    k = torch.zeros(2, 3, 7, 64, dtype=torch.bfloat16)   # [B, H, Nk, d]
+    assert _qkv_shapes(q, k, k, "bhnd") == (2, 3, 5, 7, 64)
+    qt, kt = q.transpose(1, 2).contiguous(), k.transpose(1, 2).contiguous()  # [B, N, H, d]
+    assert _qkv_shapes(qt, kt, kt, "bnhd") == (2, 3, 5, 7, 64)
+    with pytest.raises(ValueError):  # heads disagree once read in the other layout
+        _qkv_shapes(qt, k, k, "bnhd")
+    with pytest.raises(ValueError):  # k and v of different shapes
+        _qkv_shapes(q, k, q, "bhnd")
+    with pytest.raises(ValueError):  # not contiguous
+        _qkv_shapes(q.transpose(1, 2), k, k, "bhnd")
+    with pytest.raises(ValueError):  # mixed dtypes
+        _qkv_shapes(q, k.half(), k.half(), "bhnd")
+
+
+def test_causal_mode_parsing():
+    from exact_attention_forward_05_gb300 import _causal_mode
+    assert [_causal_mode(c) for c in (False, True, 0, 1, 2)] == [0, 1, 0, 1, 2]
+    assert [_causal_mode(c) for c in ("none", "top_left", "bottom_right")] == [0, 1, 2]
+    for bad in ("causal", 3, -1):
+        with pytest.raises(ValueError):
+            _causal_mode(bad)
