@@ -212,3 +212,19 @@ def test_causal_mode_parsing():
     for bad in ("causal", 3, -1):
         with pytest.raises(ValueError):
             _causal_mode(bad)
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/attn.h compiles as strict C99 and every declared function can be
+    named from C (the boundary has no C++ or torch types)."""
+    import os
+    import subprocess
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    names = attn.exported_symbols()
+    refs = ", ".join(f"(any_fn)&{n}" for n in names)
+    src = tmp_path / "use_header.c"
+    src.write_text(f'#include "attn.h"\ntypedef void (*any_fn)(void);\n'
+                   f'static const any_fn fns[] = {{{refs}}};\n'
+                   f'int main(void) {{ return (int)(sizeof fns / sizeof fns[0]) - {len(names)}; }}\n')
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", inc, "-c", str(src),
+                    "-o", str(tmp_path / "use_header.o")], check=True)
