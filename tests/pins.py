@@ -368,5 +368,18 @@ def check_bwd_unseen_keys_get_nothing(attn, bwd):
         assert np.all(x == 0)
 
 
+def check_bwd_golden(attn, bwd):
+    """Hand-worked gradients with exact expected values
+    (tests/golden/two_key_backward.json)."""
+    with open(os.path.join(GOLDEN, "two_key_backward.json")) as f:
+        cases = json.load(f)["cases"]
+    for case in cases:
+        q, k, v, g = (np.array(case[n], dtype=np.float64)[None, None] for n in ("q", "k", "v", "g"))
+        grads = bwd(q, k, v, g, 1 if case["causal"] else 0, case["scale"])
+        for name, got in zip(("dq", "dk", "dv"), grads):
+            np.testing.assert_allclose(got[0, 0], np.array(case[name]), rtol=0, atol=1e-14,
+                                       err_msg=f"{case['name']}: {name}")
+
+
 BWD_CHECKS = [check_bwd_finite_differences, check_bwd_sums, check_bwd_zero_scale,
-              check_bwd_unseen_keys_get_nothing]
+              check_bwd_unseen_keys_get_nothing, check_bwd_golden]
