@@ -98,7 +98,8 @@ _TORCH_DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16, "fp32": torch.fl
 
 
 def as_dtype(x: np.ndarray, shape, dtype: str) -> torch.Tensor:
-    """Round float64 draws to the storage dtype (round to nearest even)."""
+    """Round float64 draws to the storage dtype: to float32, then to the 16-bit
+    type, each step to nearest even."""
     t = torch.from_numpy(x.astype(np.float32, copy=False)).reshape(shape)
     return t.to(_TORCH_DTYPES[dtype]).contiguous()
 
