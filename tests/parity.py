@@ -57,6 +57,32 @@ def assert_within_rounding(o_gpu, o_ref, v, what=""):
     assert np.all(excess <= 0), f"{what}: exceeds the rounding bound by {excess.max():.3e}"
 
 
+def assert_close_elementwise(o_gpu, lse_gpu, o_ref, lse_ref, q, k, v, causal, scale, rows=None, what=""):
+    """The fixed tolerances, except that an element of O whose fixed 1e-2
+    bound is below what the kernel's two roundings allow is held to that
+    instead.  The kernel rounds every softmax weight to the 16-bit input type
+    before P V and rounds O once at the end, so element e of O may differ from
+    the exact value by u (|O_e| + A_e) with A = P |V| (the weighted mean of
+    |v|, computed by the oracle) and u the unit roundoff (2^-8 bf16, 2^-11
+    fp16), plus float32 accumulation (1e-4 allowance).  In early causal rows
+    (few keys) |O| reaches 2-4, where one bf16 rounding of O alone can exceed
+    1e-2.  RMS <= 2e-3 and max |dlse| <= 1e-3 are never relaxed, and the extra
+    oracle pass runs only when some element misses the fixed bound."""
+    m = metrics(o_gpu, lse_gpu, o_ref, lse_ref)
+    assert m["finite"], f"{what}: non-finite output"
+    assert m["rms"] <= RMS, f"{what}: RMS {m['rms']:.3e} > {RMS}"
+    assert m["lse_abs"] <= LSE_ABS, f"{what}: max |dlse| {m['lse_abs']:.3e} > {LSE_ABS}"
+    if m["max_abs"] <= MAX_ABS:
+        return m
+    u = UNIT_ROUNDOFF[o_gpu.dtype]
+    a_ref, _ = oracle.attention(q, k, v.abs(), causal=causal, scale=scale, rows=rows)
+    o = o_gpu.double().cpu().numpy()
+    bound = np.maximum(MAX_ABS, u * (np.abs(o_ref) + a_ref) + 1e-4)
+    excess = np.abs(o - o_ref) - bound
+    assert np.all(excess <= 0), f"{what}: max |dO| {m['max_abs']:.3e} exceeds the rounding bound by {excess.max():.3e}"
+    return dict(m, rounding_bound_used=True)
+
+
 def check_case(q, k, v, causal, scale=None, rows=None, what="", large_outputs=False):
     """Run the kernel, compare every output row (or the sampled ``rows``) with
     the oracle; returns the metrics.  ``large_outputs`` replaces the fixed

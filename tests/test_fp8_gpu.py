@@ -140,30 +140,34 @@ def test_fp8_weights_layout_through_identity_values():
 def test_fp8_error_against_exact_attention(N):
     """FP8 path with per-block scales and the Hadamard rotation on inputs with
     0.1 % outliers (B = 16384 / N, H = 16, d = 128): RMS <= 2.5e-2 against
-    exact attention on the 16-bit inputs (sampled rows); the naive per-tensor
-    FP8 baseline is computed on the same rows and reported."""
+    exact attention on the 16-bit inputs.  The RMS runs over 256 seeded query
+    rows of every head for N <= 4096, and over 64 rows of 8 heads spread over
+    the batch above that.  The naive per-tensor FP8 baseline is computed on the
+    same rows and reported next to it."""
     B, H = 16384 // N, 16
     q, k, v = synth.outlier_inputs(B, H, N, D, "bf16", seed=0)
     signs = synth.hadamard_signs(H, D, seed=0)
-    rows = synth.sample_rows(N, 32, seed=0, salt=N)
-    heads = [0, B * H // 2, B * H - 1]
+    if N <= 4096:
+        rows = synth.sample_rows(N, 256, seed=0, salt=N)
+        heads = list(range(B * H))
+    else:
+        rows = synth.sample_rows(N, 64, seed=0, salt=N)
+        heads = [int(i) for i in np.linspace(0, B * H - 1, 8).round()]
     qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
     o8, _ = attn.attn_fwd_fp8_pipeline(qc, kc, vc, signs=signs.cuda())
     ob, _ = attn.attn_fwd_fp8_pipeline(qc, kc, vc, signs=None, per_tensor=True)
     torch.cuda.synchronize()
+    assert bool(torch.isfinite(o8).all()) and bool(torch.isfinite(ob).all())
     flat = lambda t: t.reshape(1, B * H, N, D)
-    err8, errb = [], []
-    for h in heads:
-        sl = slice(h, h + 1)
-        o_ref, _ = oracle.attention(flat(q)[:, sl], flat(k)[:, sl], flat(v)[:, sl], scale=D ** -0.5,
-                                    rows=rows)
-        idx = torch.as_tensor(rows, device="cuda")
-        err8.append(flat(o8)[:, sl][:, :, idx].double().cpu().numpy() - o_ref)
-        errb.append(flat(ob)[:, sl][:, :, idx].double().cpu().numpy() - o_ref)
-    rms8 = float(np.sqrt(np.mean(np.concatenate(err8) ** 2)))
-    rmsb = float(np.sqrt(np.mean(np.concatenate(errb) ** 2)))
-    print(f"N={N}: FP8 per-block + Hadamard RMS {rms8:.3e}; naive per-tensor FP8 RMS {rmsb:.3e}; "
-          f"ratio {rmsb / rms8:.2f}")
+    hsel = torch.as_tensor(heads)
+    o_ref, _ = oracle.attention(flat(q)[:, hsel], flat(k)[:, hsel], flat(v)[:, hsel], scale=D ** -0.5,
+                                rows=rows)
+    idx = torch.as_tensor(rows, device="cuda")
+    pick = lambda o: flat(o)[:, hsel.cuda()][:, :, idx].double().cpu().numpy()
+    rms8 = float(np.sqrt(np.mean((pick(o8) - o_ref) ** 2)))
+    rmsb = float(np.sqrt(np.mean((pick(ob) - o_ref) ** 2)))
+    print(f"N={N}: {len(rows)} rows x {len(heads)} heads: FP8 per-block + Hadamard RMS {rms8:.3e}; "
+          f"naive per-tensor FP8 RMS {rmsb:.3e}; ratio {rmsb / rms8:.2f}")
     assert rms8 <= FP8_RMS
     assert attn.device_status() == attn.ATTN_OK
 
