@@ -61,13 +61,49 @@ def describe(w) -> str:
             f"{'causal' if w['causal'] else 'non-causal'}")
 
 
-def peaks():
+# NVIDIA's dense (no 2:4 sparsity) per-GPU tensor figures for GB300, for
+# context beside the measured denominators.
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_FP8_TFLOPS = 4500.0
+
+
+def peaks(sustained: bool = False):
+    """The bf16 denominator: the measured cuBLAS bf16 GEMM rate (burst,
+    or the seconds-long sustained loop), i.e. what cuBLAS achieves on this
+    GB300 -- below the datasheet figure."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             p = json.load(f)
-        return float(p["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+        if sustained and "bf16_tflops_sustained" in p:
+            return float(p["bf16_tflops_sustained"]), \
+                "measured cuBLAS bf16 GEMM, sustained (MEASURED_PEAKS.json bf16_tflops_sustained; cuBLAS-achievable, not the datasheet peak)"
+        return float(p["bf16_tflops"]), \
+            "measured cuBLAS bf16 GEMM, burst (MEASURED_PEAKS.json bf16_tflops; cuBLAS-achievable, not the datasheet peak)"
     return FALLBACK_BF16_TFLOPS, "fallback (1.9 PFLOP/s bf16 burst, one earlier GB300 measurement)"
+
+
+def hbm_peak() -> float:
+    """Measured copy bandwidth (MEASURED_PEAKS.json hbm_gbs), else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"])
+    return 6800.0
+
+
+def roofline(achieved, fp8=False, sustained=False, **extra):
+    """Roofline object: `peak` is the measured denominator (FP8: twice the
+    measured bf16 rate, the nominal FP8/BF16 ratio of the tensor cores);
+    `frac_nominal` is the same rate against NVIDIA's dense datasheet figure."""
+    peak, src = peaks(sustained)
+    if fp8:
+        peak, src = 2.0 * peak, "2 x " + src + " (nominal FP8 / BF16 dense ratio)"
+    nominal = NOMINAL_FP8_TFLOPS if fp8 else NOMINAL_BF16_TFLOPS
+    return dict({"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": UNIT,
+                 "frac": round(achieved / peak, 4), "peak_source": src, "peak_nominal": nominal,
+                 "frac_nominal": round(achieved / nominal, 4),
+                 "peak_nominal_source": "NVIDIA GB300 dense tensor figure (no sparsity)"}, **extra)
 
 
 def dist_env():
@@ -79,16 +115,64 @@ def dist_env():
 
 # ------------------------------------------------------------------ clocks
 
+REASON_BITS = {  # NVML clocks-event reason bits
+    "sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+    "hw_power_brake_slowdown": 0x80}
+
+
+class _Nvml:
+    """Read-only NVML queries through ctypes (SM clock, its maximum, power,
+    clocks-event reasons).  Nothing here changes a GPU setting."""
+
+    def __init__(self, device_index: int):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+        ident = (uuid if uuid.startswith("GPU-") else f"GPU-{uuid}").encode()
+        if self.lib.nvmlDeviceGetHandleByUUID(ctypes.c_char_p(ident), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle for the device")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.max_sm = self._clock(self.lib.nvmlDeviceGetMaxClockInfo)
+
+    def _clock(self, fn):
+        v = self.ct.c_uint()
+        return float(v.value) if fn(self.h, 1, self.ct.byref(v)) == 0 else None  # 1 = SM clock
+
+    def sample(self):
+        """(sm_mhz, sm_max_mhz, power_w, reasons bitmask)"""
+        p, r = self.ct.c_uint(), self.ct.c_ulonglong()
+        pw = p.value / 1000.0 if self.lib.nvmlDeviceGetPowerUsage(self.h, self.ct.byref(p)) == 0 else None
+        rs = r.value if self.reasons_fn(self.h, self.ct.byref(r)) == 0 else 0
+        return self._clock(self.lib.nvmlDeviceGetClockInfo), self.max_sm, pw, rs
+
+
 class ClockSampler:
-    """nvidia-smi samples (every 100 ms) with host timestamps."""
+    """Clock samples with host timestamps, taken every 2 ms through NVML
+    (every 100 ms through nvidia-smi when NVML cannot be loaded)."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int):
-        self.samples = []
+    def __init__(self, device_index: int, period_s: float = 0.002):
+        self.samples = []  # (time, sm_mhz, sm_max_mhz, power_w, {reason names})
         self.proc = None
+        self.source = None
+        self._stop = threading.Event()
+        try:
+            nv = _Nvml(device_index)
+            nv.sample()
+            self.source = "nvml 2 ms"
+            self.thread = threading.Thread(target=self._poll, args=(nv, period_s), daemon=True)
+            self.thread.start()
+            return
+        except Exception:
+            pass
         try:
             uuid = str(torch.cuda.get_device_properties(device_index).uuid)
             ident = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
@@ -101,14 +185,43 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             return
+        self.source = "nvidia-smi 100 ms"
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
 
+    def _poll(self, nv, period_s):
+        while not self._stop.is_set():
+            try:
+                sm, mx, pw, bits = nv.sample()
+            except Exception:
+                return
+            if sm is not None:
+                self.samples.append((time.time(), sm, mx, pw,
+                                     {n for n, b in REASON_BITS.items() if bits & b}))
+            time.sleep(period_s)
+
     def _read(self):
         for line in self.proc.stdout:
-            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+            self.add_smi_line(time.time(), line)
+
+    def add_smi_line(self, ts, line):
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 7:
+            return
+        try:
+            sm, mx = float(f[0]), float(f[1])
+        except ValueError:
+            return
+        try:
+            pw = float(f[2])
+        except ValueError:
+            pw = None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = {n for n, val in zip(names, f[3:7]) if val.lower().startswith("active")}
+        self.samples.append((ts, sm, mx, pw, reasons))
 
     def stop(self):
+        self._stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -117,23 +230,21 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self, t0: float, t1: float):
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        sm, mx, reasons = [], [], set()
-        for ts, f in self.samples:
-            if not (t0 <= ts <= t1) or len(f) < 7:
+        sm, mx, pw, reasons = [], [], [], set()
+        for ts, s_mhz, m_mhz, p_w, rs in list(self.samples):
+            if not (t0 <= ts <= t1):
                 continue
-            try:
-                sm.append(float(f[0]))
-                mx.append(float(f[1]))
-            except ValueError:
-                continue
-            for name, val in zip(names, f[3:7]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
+            sm.append(s_mhz)
+            if m_mhz is not None:
+                mx.append(m_mhz)
+            if p_w is not None:
+                pw.append(p_w)
+            reasons |= rs
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": self.source}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
+                "sm_min_mhz": min(sm), "power_w_max": max(pw) if pw else None,
+                "reasons": sorted(reasons), "samples": len(sm), "source": self.source}
 
 
 # --------------------------------------------------------------- GPU arm
@@ -149,6 +260,19 @@ def time_kernel(fn, steps: int, warmup: int, stream):
     ev[1].record(stream)
     torch.cuda.synchronize()
     return ev[0].elapsed_time(ev[1])  # ms
+
+
+def time_for(fn, seconds: float, stream, sampler=None, min_steps: int = 3):
+    """Back-to-back launches for at least `seconds` of device time, in
+    batches timed with CUDA events on `stream`; returns (ms per launch,
+    launches, clocks of the window)."""
+    ms = time_kernel(fn, 3, 0, stream) / 3  # estimate
+    n = max(min_steps, int(seconds * 1e3 / max(ms, 1e-3)))
+    t0 = time.time()
+    total = time_kernel(fn, n, 0, stream)
+    t1 = time.time()
+    clocks = sampler.summary(t0, t1) if sampler else None
+    return total / n, n, clocks
 
 
 def barrier(world):
@@ -278,16 +402,24 @@ def run_gpu(args):
     per_step = ms_max / args.steps
     value = flops(w) * world / (per_step * 1e-3) / 1e12
 
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+
+    # The same launch back to back for at least 1.5 s: its clocks (power cap
+    # included) and its rate against the sustained cuBLAS denominator.
+    ms_sus, n_sus, clocks_sus = time_for(step, 1.5, stream, sampler)
+    ms_sus = max_over_ranks(ms_sus, world)
+    sus_value = flops(w) / (ms_sus * 1e-3) / 1e12
+
     # the other mask setting of the same shapes, for context
     other = dict(w, causal=not w["causal"])
-    ms_o = max_over_ranks(time_kernel(lambda: step(other["causal"]), max(args.steps // 4, 3), 3,
-                                      stream), world)
-    other_value = flops(other) * world / (ms_o / max(args.steps // 4, 3) * 1e-3) / 1e12
+    ms_o, _, clocks_o = time_for(lambda: step(other["causal"]), 0.3, stream, sampler)
+    ms_o = max_over_ranks(ms_o, world)
+    other_value = flops(other) * world / (ms_o * 1e-3) / 1e12
     step()  # leave o / lse for the configured mask
     torch.cuda.synchronize()
-    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
-    if sampler:
-        sampler.stop()
+    status = attn.device_status()
+    if status != attn.ATTN_OK:
+        raise RuntimeError(f"device status {attn.status_string(status)}")
 
     # end to end: host buffers (pinned) through the C ABI, copies in the timed region
     qp, kp, vp = q.pin_memory(), k.pin_memory(), v.pin_memory()
@@ -306,9 +438,11 @@ def run_gpu(args):
     e2e_s = max_over_ranks(time.perf_counter() - t0, world) / e2e_steps
     e2e_value = flops(w) * world / e2e_s / 1e12
 
-    fp8 = fp8_leg(w, dev, stream, rank, args) if w["d"] == 128 else None
+    fp8 = fp8_leg(w, dev, stream, rank, args, sampler) if w["d"] == 128 else None
+    host = host_cost(dev, stream) if rank == 0 else None
+    if sampler:
+        sampler.stop()
 
-    peak, peak_src = peaks()
     achieved = flops(w) / (ms / args.steps * 1e-3) / 1e12
     line = None
     if rank == 0:
@@ -325,10 +459,7 @@ def run_gpu(args):
                        "flops_per_step_per_gpu": flops(w),
                        "l2": "inputs larger than L2 (Q, K, V, O = 4 x %.0f MiB)" % (B * H * N * d * 2 / 2 ** 20),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-            "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
-                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                         "peak_source": peak_src, "traffic": traffic_from_profile(),
-                         "kernel": "attn_fwd_kernel<128, bf16>"},
+            "roofline": roofline(achieved, traffic=traffic_from_profile(), kernel="attn_fwd_kernel<128, bf16>"),
             "cpu_baseline": {k2: (round(v2, 6) if isinstance(v2, float) else v2)
                              for k2, v2 in cpu.items() if k2 != "seconds"},
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
@@ -337,8 +468,13 @@ def run_gpu(args):
                     "path": "attn_fwd_host (pinned host buffers)"},
             "gpu_launches": n_launch,
             "clocks": clocks,
-            "other_mask": {"causal": other["causal"], "value": round(other_value, 2), "unit": UNIT},
+            "sustained": {"value": round(sus_value, 2), "unit": UNIT, "launches": n_sus,
+                          "seconds": round(ms_sus * n_sus / 1e3, 2),
+                          "roofline": roofline(sus_value, sustained=True), "clocks": clocks_sus},
+            "other_mask": {"causal": other["causal"], "value": round(other_value, 2), "unit": UNIT,
+                           "clocks": clocks_o},
             "fp8": fp8,
+            "host": host,
             "parity_sample": par,
             "device": torch.cuda.get_device_name(dev),
         }
@@ -348,14 +484,44 @@ def run_gpu(args):
     return line
 
 
-def fp8_leg(w, dev, stream, rank, args):
+def host_cost(dev, stream, calls: int = 500):
+    """Host time per attn_fwd call in the library (C ABI called directly
+    through ctypes, arguments marshalled once; the GPU is left to drain the
+    launches after the loop) on the smallest sweep point, bf16 B=32, H=16,
+    N=512, d=128, beside that launch's device time."""
+    import ctypes
+    import exact_attention_forward_05_gb300 as attn
+    B, H, N, d = 32, 16, 512, 128
+    q = torch.randn(B, H, N, d, device=dev, dtype=torch.bfloat16)
+    k, v, o = torch.randn_like(q), torch.randn_like(q), torch.empty_like(q)
+    lse = torch.empty(B, H, N, device=dev, dtype=torch.float32)
+    lib = attn.lib()
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, 0,
+            ctypes.c_float(d ** -0.5), attn.ATTN_BF16, ctypes.c_void_p(stream.cuda_stream))
+    for _ in range(10):
+        lib.attn_fwd(*args)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(calls):
+        lib.attn_fwd(*args)
+    host_us = (time.perf_counter() - t0) / calls * 1e6
+    torch.cuda.synchronize()
+    dev_us = time_kernel(lambda: lib.attn_fwd(*args), 200, 0, stream) / 200 * 1e3
+    return {"workload": "bf16 attention fwd, B=32, H=16, N=512, d=128, non-causal",
+            "host_us_per_call": round(host_us, 2), "device_us_per_launch": round(dev_us, 2),
+            "note": "host time of the C entry point per call (argument checks, cached tensor maps, launch)"}
+
+
+def fp8_leg(w, dev, stream, rank, args, sampler=None):
     """The FP8 path on the same shapes with 0.1 % outliers in Q, K, V: the FP8
     attention kernel alone (against the FP8 dense peak = 2 x the measured bf16
     peak, the nominal FP8/BF16 ratio of the tensor cores), the pre-pass
     (Hadamard rotation + block quantisation, HBM-bound), the pre-pass with the
     rotary embedding of Q and K fused in front, and pre-pass + kernel together;
     plus the RMS error against exact attention on sampled rows next to the
-    naive per-tensor FP8 baseline."""
+    naive per-tensor FP8 baseline.  The kernel is timed over the same number
+    of back-to-back launches as the main line (a burst, like the bf16 figure)
+    and again for 1.5 s (sustained); every timing carries its clock record."""
     import exact_attention_forward_05_gb300 as attn
     import synth
     B, H, N, d = w["B"], w["H"], w["N"], w["d"]
@@ -375,27 +541,39 @@ def fp8_leg(w, dev, stream, rank, args):
     def both():
         prep()
         fwd()
-    n = max(args.steps // 4, 5)
     prep()
-    t_fwd = time_kernel(fwd, n, 3, stream) / n
-    t_prep = time_kernel(prep, n, 3, stream) / n
-    t_prep_rope = time_kernel(prep_rope, n, 3, stream) / n
-    t_both = time_kernel(both, n, 3, stream) / n
+    for _ in range(3):
+        fwd()
+    torch.cuda.synchronize()
+    n = max(args.steps, 20)
+    t0 = time.time()
+    t_fwd = time_kernel(fwd, n, 0, stream) / n
+    clocks_fwd = sampler.summary(t0, time.time()) if sampler else None
+    t_sus, n_sus, clocks_sus = time_for(fwd, 1.5, stream, sampler)
+    t_prep, _, clocks_prep = time_for(prep, 0.3, stream, sampler)
+    t_prep_rope, _, _ = time_for(prep_rope, 0.3, stream, sampler)
+    t_both, _, _ = time_for(both, 0.3, stream, sampler)
     if attn.device_status() != attn.ATTN_OK:
         raise RuntimeError("device status after the FP8 leg")
-    peak = 2.0 * peaks()[0]
     fl = flops(w)
+    val = fl / (t_fwd * 1e-3) / 1e12
+    sus = fl / (t_sus * 1e-3) / 1e12
+    prep_bytes = 3 * q.numel() * 2 + 3 * q.numel() + 3 * B * H * nblk * 4
     out = {"workload": f"fp8 e4m3 attention fwd, B={B}, H={H}, N={N}, d={d}, "
                        f"{'causal' if w['causal'] else 'non-causal'}, per-block scales + Hadamard, "
                        "inputs N(0,1) + N(0,100) * Bernoulli(0.001), bf16 output",
-           "value": round(fl / (t_fwd * 1e-3) / 1e12, 2), "unit": UNIT,
-           "roofline": {"bound": "tensor", "achieved": round(fl / (t_fwd * 1e-3) / 1e12, 2),
-                        "peak": peak, "frac": round(fl / (t_fwd * 1e-3) / 1e12 / peak, 4),
-                        "peak_source": "2 x measured bf16 burst (nominal FP8 / BF16 dense ratio)",
-                        "kernel": "attn_fwd_kernel<128, e4m3>"},
+           "value": round(val, 2), "unit": UNIT, "launches": n,
+           "roofline": roofline(val, fp8=True, kernel="attn_fwd_kernel<128, e4m3>"),
+           "clocks": clocks_fwd,
+           "sustained": {"value": round(sus, 2), "launches": n_sus, "roofline": roofline(sus, fp8=True, sustained=True),
+                         "clocks": clocks_sus},
            "prepare_us": round(t_prep * 1e3, 2),
            "prepare_rotary_us": round(t_prep_rope * 1e3, 2),
-           "prepare_gbs": round((3 * q.numel() * 2 + 3 * q.numel() + 3 * B * H * nblk * 4) / (t_prep * 1e-3) / 1e9, 1),
+           "prepare_gbs": round(prep_bytes / (t_prep * 1e-3) / 1e9, 1),
+           "prepare_roofline": {"bound": "hbm", "achieved": round(prep_bytes / (t_prep * 1e-3) / 1e9, 1),
+                                "peak": hbm_peak(), "unit": "GB/s",
+                                "frac": round(prep_bytes / (t_prep * 1e-3) / 1e9 / hbm_peak(), 4),
+                                "algorithmic_bytes": prep_bytes, "clocks": clocks_prep},
            "pipeline_value": round(fl / (t_both * 1e-3) / 1e12, 2)}
     if rank == 0:
         import oracle
@@ -464,12 +642,14 @@ def run_ablation(args):
     """Overlap ablation (in the spirit of the FlashAttention-3 page's ablation
     table): the bench workload, causal and not, and the FP8 kernel, timed with
     two Q tiles per CTA whose softmax and products overlap (ping-pong, the
-    default) and with one Q tile per CTA at a time (no overlap)."""
+    default) and with one Q tile per CTA at a time (no overlap).  Each line is
+    at least 0.5 s of back-to-back launches and carries its clock record."""
     import exact_attention_forward_05_gb300 as attn
     import synth
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream(dev)
-    peak = peaks()[0]
+    sampler = ClockSampler(0)
+    time.sleep(0.5)
     B, H, N, d = 2, 16, 8192, 128
     q, k, v = (t.to(dev) for t in synth.attention_inputs(B, H, N, d, "bf16", seed=0))
     o = torch.empty_like(q)
@@ -477,27 +657,31 @@ def run_ablation(args):
     qo, ko, vo = (t.to(dev) for t in synth.outlier_inputs(B, H, N, d, "bf16", seed=0))
     bufs = attn.fp8_prepare(qo, ko, vo, signs=synth.hadamard_signs(H, d, seed=0).to(dev))
     o8 = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+
+    def emit(name, w, f, fp8):
+        for _ in range(max(args.warmup, 3)):
+            f()
+        ms, n, clocks = time_for(f, 0.5, stream, sampler)
+        tf = flops(w) / (ms * 1e-3) / 1e12
+        rl = roofline(tf, fp8=fp8)
+        print(json.dumps({"schedule": name, "workload": describe(w), "value": round(tf, 1), "unit": UNIT,
+                          "frac": rl["frac"], "frac_nominal": rl["frac_nominal"], "ms": round(ms, 4),
+                          "launches": n, "clocks": clocks}), flush=True)
+
     try:
         for mode, name in ((attn.SCHEDULE_PINGPONG, "ping-pong (two Q tiles, overlap)"),
                            (attn.SCHEDULE_ONE_TILE, "one Q tile per CTA (no overlap)")):
             attn.set_schedule(mode)
             for causal in (False, True):
-                f = lambda: attn.attn_fwd(q, k, v, causal=causal, scale=d ** -0.5, out=o, lse=lse,
-                                          stream=stream)
-                w = dict(B=B, H=H, N=N, d=d, causal=causal, dtype="bf16")
-                ms = time_kernel(f, args.steps, args.warmup, stream) / args.steps
-                tf = flops(w) / (ms * 1e-3) / 1e12
-                print(json.dumps({"schedule": name, "workload": describe(w), "value": round(tf, 1),
-                                  "unit": UNIT, "frac": round(tf / peak, 4), "ms": round(ms, 4)}), flush=True)
-            f = lambda: attn.attn_fwd_fp8(*bufs, causal=False, scale=d ** -0.5, out=o8,
-                                          return_lse=False, stream=stream)
-            w = dict(B=B, H=H, N=N, d=d, causal=False, dtype="fp8 e4m3")
-            ms = time_kernel(f, args.steps, args.warmup, stream) / args.steps
-            tf = flops(w) / (ms * 1e-3) / 1e12
-            print(json.dumps({"schedule": name, "workload": describe(w), "value": round(tf, 1),
-                              "unit": UNIT, "frac": round(tf / (2 * peak), 4), "ms": round(ms, 4)}), flush=True)
+                emit(name, dict(B=B, H=H, N=N, d=d, causal=causal, dtype="bf16"),
+                     lambda: attn.attn_fwd(q, k, v, causal=causal, scale=d ** -0.5, out=o, lse=lse,
+                                           stream=stream), False)
+            emit(name, dict(B=B, H=H, N=N, d=d, causal=False, dtype="fp8 e4m3"),
+                 lambda: attn.attn_fwd_fp8(*bufs, causal=False, scale=d ** -0.5, out=o8,
+                                           return_lse=False, stream=stream), True)
     finally:
         attn.set_schedule(attn.SCHEDULE_PINGPONG)
+        sampler.stop()
     if attn.device_status() != attn.ATTN_OK:
         raise RuntimeError("device status after the ablation")
 
@@ -506,49 +690,56 @@ def run_sweep(args):
     """One device-timed line per point of the sequence-length sweep (bf16,
     B = 16384/N, H = 2048/d, causal and non-causal), the FP8 kernel at
     d = 128 (H = 16, inputs with 0.1 % outliers), and the long-context causal
-    case (B = 1, H = 16, N = 32768, d = 128).  Same timing as the main
-    line: CUDA events on the launching stream around ``--steps`` launches."""
+    case (B = 1, H = 16, N = 32768, d = 128).  Each point: CUDA events on the
+    launching stream around at least 0.5 s of back-to-back launches, with the
+    clock record of that window."""
     import exact_attention_forward_05_gb300 as attn
     import synth
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream(dev)
-    peak = peaks()[0]
+    sampler = ClockSampler(0)
+    time.sleep(0.5)
 
-    def emit(w, ms, pk):
+    def emit(w, f, fp8=False):
+        for _ in range(max(args.warmup, 3)):
+            f()
+        ms, n, clocks = time_for(f, 0.5, stream, sampler)
         tf = flops(w) / (ms * 1e-3) / 1e12
+        rl = roofline(tf, fp8=fp8)
         print(json.dumps({"workload": describe(w), "value": round(tf, 1), "unit": UNIT,
-                          "frac": round(tf / pk, 4), "ms": round(ms, 4)}), flush=True)
+                          "frac": rl["frac"], "frac_nominal": rl["frac_nominal"], "ms": round(ms, 4),
+                          "launches": n, "clocks": clocks}), flush=True)
 
-    for N in (512, 1024, 2048, 4096, 8192, 16384):
-        for d in (64, 128, 256):
-            B, H = 16384 // N, 2048 // d
-            q, k, v = (t.to(dev) for t in synth.attention_inputs(B, H, N, d, "bf16", seed=0))
-            o = torch.empty_like(q)
-            lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    try:
+        for N in (512, 1024, 2048, 4096, 8192, 16384):
+            for d in (64, 128, 256):
+                B, H = 16384 // N, 2048 // d
+                q, k, v = (t.to(dev) for t in synth.attention_inputs(B, H, N, d, "bf16", seed=0))
+                o = torch.empty_like(q)
+                lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+                for causal in (False, True):
+                    emit(dict(B=B, H=H, N=N, d=d, causal=causal, dtype="bf16"),
+                         lambda: attn.attn_fwd(q, k, v, causal=causal, scale=d ** -0.5, out=o, lse=lse,
+                                               stream=stream))
+                del q, k, v, o, lse
+            B, H, d = 16384 // N, 16, 128
+            q, k, v = (t.to(dev) for t in synth.outlier_inputs(B, H, N, d, "bf16", seed=0))
+            bufs = attn.fp8_prepare(q, k, v, signs=synth.hadamard_signs(H, d, seed=0).to(dev))
+            o8 = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
             for causal in (False, True):
-                f = lambda: attn.attn_fwd(q, k, v, causal=causal, scale=d ** -0.5, out=o, lse=lse,
-                                          stream=stream)
-                emit(dict(B=B, H=H, N=N, d=d, causal=causal, dtype="bf16"),
-                     time_kernel(f, args.steps, args.warmup, stream) / args.steps, peak)
-            del q, k, v, o, lse
-        B, H, d = 16384 // N, 16, 128
-        q, k, v = (t.to(dev) for t in synth.outlier_inputs(B, H, N, d, "bf16", seed=0))
-        bufs = attn.fp8_prepare(q, k, v, signs=synth.hadamard_signs(H, d, seed=0).to(dev))
-        o8 = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
-        for causal in (False, True):
-            f = lambda: attn.attn_fwd_fp8(*bufs, causal=causal, scale=d ** -0.5, out=o8,
-                                          return_lse=False, stream=stream)
-            emit(dict(B=B, H=H, N=N, d=d, causal=causal, dtype="fp8 e4m3"),
-                 time_kernel(f, args.steps, args.warmup, stream) / args.steps, 2 * peak)
-    # Long-context configuration: B = 1, H = 16, N = 32768, d = 128, causal.
-    B, H, N, d = 1, 16, 32768, 128
-    q, k, v = (t.to(dev) for t in synth.attention_inputs(B, H, N, d, "bf16", seed=0))
-    o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    f = lambda: attn.attn_fwd(q, k, v, causal=True, scale=d ** -0.5, out=o, lse=lse, stream=stream)
-    emit(dict(B=B, H=H, N=N, d=d, causal=True, dtype="bf16"),
-         time_kernel(f, args.steps, args.warmup, stream) / args.steps, peak)
-    del q, k, v, o, lse
+                emit(dict(B=B, H=H, N=N, d=d, causal=causal, dtype="fp8 e4m3"),
+                     lambda: attn.attn_fwd_fp8(*bufs, causal=causal, scale=d ** -0.5, out=o8,
+                                               return_lse=False, stream=stream), fp8=True)
+        # Long-context configuration: B = 1, H = 16, N = 32768, d = 128, causal.
+        B, H, N, d = 1, 16, 32768, 128
+        q, k, v = (t.to(dev) for t in synth.attention_inputs(B, H, N, d, "bf16", seed=0))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        emit(dict(B=B, H=H, N=N, d=d, causal=True, dtype="bf16"),
+             lambda: attn.attn_fwd(q, k, v, causal=True, scale=d ** -0.5, out=o, lse=lse, stream=stream))
+        del q, k, v, o, lse
+    finally:
+        sampler.stop()
     if attn.device_status() != attn.ATTN_OK:
         raise RuntimeError("device status after the sweep")
 
