@@ -22,7 +22,8 @@ import torch
 from . import build as _build
 
 __all__ = ["attn_fwd", "attn_fwd_host", "fp8_prepare", "attn_fwd_fp8", "attn_fwd_fp8_pipeline", "host_workspace_bytes", "device_status",
-           "set_wait_timeout_ns", "set_schedule", "debug_bounded_wait", "status_string", "library_path",
+           "set_wait_timeout_ns", "set_schedule", "debug_bounded_wait", "debug_fail_host_chunk", "debug_exp2_poly",
+           "attn_fwd_host_noalloc", "status_string", "library_path",
            "AttnError", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
            "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "exported_symbols",
            "LAYOUT_BHND", "LAYOUT_BNHD", "CAUSAL_NONE", "CAUSAL_TOP_LEFT", "CAUSAL_BOTTOM_RIGHT"]
@@ -94,6 +95,12 @@ def _load():
             lib.attn_set_schedule.argtypes = [i32]
             lib.attn_debug_bounded_wait.argtypes = [u64, vp]
             lib.attn_debug_bounded_wait.restype = i32
+            lib.attn_debug_exp2_poly.argtypes = [vp, vp, vp, i32, vp]
+            lib.attn_debug_exp2_poly.restype = i32
+            lib.attn_debug_fail_host_chunk.argtypes = [i32]
+            lib.attn_debug_fail_host_chunk.restype = None
+            lib.attn_fwd_host_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp]
+            lib.attn_fwd_host_noalloc.restype = i32
             lib.attn_last_cuda_error.argtypes = []
             lib.attn_last_cuda_error.restype = i32
             lib.attn_status_string.argtypes = [i32]
@@ -339,6 +346,24 @@ def set_schedule(mode: int) -> None:
     _check(_load().attn_set_schedule(int(mode)), "attn_set_schedule")
 
 
+def debug_exp2_poly(x: torch.Tensor):
+    """(polynomial 2^x of the FP8 weights, CUDA exp2f) of a float32 CUDA
+    tensor, elementwise (a test hook)."""
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 CUDA tensor")
+    yp, yr = torch.empty_like(x), torch.empty_like(x)
+    with torch.cuda.device(x.device):
+        _check(_load().attn_debug_exp2_poly(x.data_ptr(), yp.data_ptr(), yr.data_ptr(), x.numel(),
+                                            _stream_handle(None, x.device)), "attn_debug_exp2_poly")
+    return yp, yr
+
+
+def debug_fail_host_chunk(chunk: int) -> None:
+    """Arm (chunk >= 0) or disarm (-1) the one-shot host-side failure of the
+    next host-buffer call at pipeline chunk ``chunk`` (a test hook)."""
+    _load().attn_debug_fail_host_chunk(int(chunk))
+
+
 def debug_bounded_wait(timeout_ns: int, stream=None) -> None:
     dev = torch.cuda.current_device()
     _check(_load().attn_debug_bounded_wait(int(timeout_ns), _stream_handle(stream, dev)),
@@ -370,9 +395,6 @@ def attn_fwd_host_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cau
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=q.is_pinned())
     fn = _load().attn_fwd_host_noalloc
-    vp, i32 = ctypes.c_void_p, ctypes.c_int
-    fn.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32, vp]
-    fn.restype = i32
     with torch.cuda.device(device):
         st = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, d,
                 int(bool(causal)), float(scale), _DTYPES[q.dtype], _stream_handle(stream, device))

@@ -18,7 +18,7 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libattn_gb300.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
 SOURCES = ["host_common.cu", "attn_fwd.cu", "attn_fp8.cu"]
-HEADERS = ["sm103.cuh", "host_common.h", "attn_kernel.cuh"]
+HEADERS = ["sm103.cuh", "host_common.h", "attn_kernel.cuh", "tmap_cache.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",

@@ -23,6 +23,8 @@ using attn_kernel::FwdParams;
 using attn_kernel::KIND_E4M3;
 using sm103::fadd2;
 using sm103::ffma2;
+using sm103::fmul2;
+using sm103::fsub2;
 
 namespace {
 
@@ -44,20 +46,6 @@ struct PrepParams {
   int H, N, nblk;
 };
 
-// Paired float32 arithmetic (one instruction for two lanes of a register pair,
-// each rounded as the scalar operation would be).
-__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
-  unsigned long long d;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(*reinterpret_cast<unsigned long long*>(&a)),
-      "l"(*reinterpret_cast<unsigned long long*>(&b)));
-  return *reinterpret_cast<float2*>(&d);
-}
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
-  unsigned long long d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(*reinterpret_cast<unsigned long long*>(&a)),
-      "l"(*reinterpret_cast<unsigned long long*>(&b)));
-  return *reinterpret_cast<float2*>(&d);
-}
 __device__ __forceinline__ float2 pair(const float (&x)[32], int e) { return make_float2(x[e], x[e + 1]); }
 __device__ __forceinline__ void put(float (&x)[32], int e, float2 v) {
   x[e] = v.x;

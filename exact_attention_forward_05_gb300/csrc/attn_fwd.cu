@@ -1,6 +1,7 @@
 // attn_fwd.cu -- C ABI of the 16-bit (fp16 / bf16) exact attention forward:
 // argument checks and dispatch to attn_kernel::attn_fwd_kernel<D, kind>
 // (attn_kernel.cuh), the host-buffer entry point, and the bounded-wait probe.
+#include <atomic>
 #include <cmath>
 #include <mutex>
 
@@ -39,6 +40,22 @@ __global__ void debug_wait_kernel(uint64_t timeout_ns) {
     mbar_wait(smem_u32(&bar), 0, wc, attn_internal::kStatusTimeoutDebug);  // nothing arrives
   }
   __syncthreads();
+}
+
+// Evaluates exp2_poly2 (the FMA-pipe 2^x of the FP8 weights) and, beside it,
+// CUDA's exp2f, on n values: thread i takes elements 2i and 2i + 1.
+__global__ void debug_exp2_kernel(const float* x, float* y_poly, float* y_ref, int n) {
+  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const bool two = i + 1 < n;
+  const float2 v = make_float2(x[i], two ? x[i + 1] : x[i]);
+  const float2 r = exp2_poly2(v);
+  y_poly[i] = r.x;
+  y_ref[i] = exp2f(v.x);
+  if (two) {
+    y_poly[i + 1] = r.y;
+    y_ref[i + 1] = exp2f(v.y);
+  }
 }
 
 attn_status check_args(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -100,6 +117,10 @@ ATTN_EXPORT attn_status attn_fwd(const void* q, const void* k, const void* v, vo
 }
 
 namespace {
+
+// Test hook (attn_debug_fail_host_chunk): chunk index at which the next
+// attn_fwd_host call stops as if that chunk's launch had failed; -1 = off.
+std::atomic<int> g_fail_chunk{-1};
 
 // Streams and events of the host-buffer pipeline, created once per device.
 constexpr int kHostChunks = 8;
@@ -175,11 +196,19 @@ ATTN_EXPORT attn_status attn_fwd_host(const void* q_host, const void* k_host, co
   const int BH = B * H;
   const int nchunk = BH < kHostChunks ? BH : kHostChunks;
   const size_t row_bytes = static_cast<size_t>(N) * d * 2;  // one (batch, head) of Q/K/V/O
+  const int fail_at = g_fail_chunk.exchange(-1);
   cudaError_t e;
+  // On any failure, whatever was already enqueued on the pipeline streams
+  // (copies into the caller's workspace and host buffers, kernels) finishes
+  // before the call returns and the streams are handed to the next call.
+  auto drain = [&](attn_status failed) {
+    for (int i = 0; i < 3; ++i) cudaStreamSynchronize(hp->st[i]);
+    return failed;
+  };
   // Work already queued on the caller's stream comes first.
-  if ((e = cudaEventRecord(hp->start, s)) != cudaSuccess) return attn_internal::cuda_status(e);
+  if ((e = cudaEventRecord(hp->start, s)) != cudaSuccess) return drain(attn_internal::cuda_status(e));
   for (int i = 0; i < 3; ++i)
-    if ((e = cudaStreamWaitEvent(hp->st[i], hp->start, 0)) != cudaSuccess) return attn_internal::cuda_status(e);
+    if ((e = cudaStreamWaitEvent(hp->st[i], hp->start, 0)) != cudaSuccess) return drain(attn_internal::cuda_status(e));
   for (int c = 0; c < nchunk; ++c) {
     const int bh0 = static_cast<int>(static_cast<int64_t>(BH) * c / nchunk);
     const int bh1 = static_cast<int>(static_cast<int64_t>(BH) * (c + 1) / nchunk);
@@ -189,25 +218,37 @@ ATTN_EXPORT attn_status attn_fwd_host(const void* q_host, const void* k_host, co
         (e = cudaMemcpyAsync(dv + off, hv + off, len, cudaMemcpyHostToDevice, hp->st[0])) != cudaSuccess ||
         (e = cudaEventRecord(hp->in[c], hp->st[0])) != cudaSuccess ||
         (e = cudaStreamWaitEvent(hp->st[1], hp->in[c], 0)) != cudaSuccess)
-      return attn_internal::cuda_status(e);
+      return drain(attn_internal::cuda_status(e));
+    if (c == fail_at) return drain(ATTN_ERR_CUDA);  // test hook: this chunk's launch "fails"
     st = attn_fwd(dq + off, dk + off, dv + off, dout + off,
                   lse_host ? dlse + static_cast<size_t>(N) * bh0 : nullptr, 1, bh1 - bh0, N, d, causal,
                   scale, dtype, hp->st[1]);
-    if (st != ATTN_OK) return st;
+    if (st != ATTN_OK) return drain(st);
     if ((e = cudaEventRecord(hp->done[c], hp->st[1])) != cudaSuccess ||
         (e = cudaStreamWaitEvent(hp->st[2], hp->done[c], 0)) != cudaSuccess ||
         (e = cudaMemcpyAsync(ho + off, dout + off, len, cudaMemcpyDeviceToHost, hp->st[2])) != cudaSuccess)
-      return attn_internal::cuda_status(e);
+      return drain(attn_internal::cuda_status(e));
     if (lse_host &&
         (e = cudaMemcpyAsync(lse_host + static_cast<size_t>(N) * bh0, dlse + static_cast<size_t>(N) * bh0,
                              static_cast<size_t>(N) * (bh1 - bh0) * 4, cudaMemcpyDeviceToHost, hp->st[2])) !=
             cudaSuccess)
-      return attn_internal::cuda_status(e);
+      return drain(attn_internal::cuda_status(e));
   }
   for (int i = 0; i < 3; ++i)
-    if ((e = cudaStreamSynchronize(hp->st[i])) != cudaSuccess) return attn_internal::cuda_status(e);
+    if ((e = cudaStreamSynchronize(hp->st[i])) != cudaSuccess) return drain(attn_internal::cuda_status(e));
   return attn_internal::cuda_status(cudaStreamSynchronize(s));
 }
+
+ATTN_EXPORT attn_status attn_debug_exp2_poly(const float* x, float* y_poly, float* y_ref, int n, void* stream) {
+  if (n < 0) return ATTN_ERR_INVALID_ARG;
+  if (n == 0) return ATTN_OK;
+  if (!x || !y_poly || !y_ref) return ATTN_ERR_INVALID_ARG;
+  const int pairs = (n + 1) / 2;
+  debug_exp2_kernel<<<(pairs + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, y_poly, y_ref, n);
+  return attn_internal::cuda_status(cudaGetLastError());
+}
+
+ATTN_EXPORT void attn_debug_fail_host_chunk(int chunk) { g_fail_chunk.store(chunk < 0 ? -1 : chunk); }
 
 ATTN_EXPORT attn_status attn_debug_bounded_wait(uint64_t timeout_ns, void* stream) {
   debug_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(timeout_ns);

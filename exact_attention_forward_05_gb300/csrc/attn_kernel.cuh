@@ -58,6 +58,7 @@
 #include <cuda_fp8.h>
 
 #include <cmath>
+#include <type_traits>
 
 #include "host_common.h"
 #include "sm103.cuh"
@@ -77,6 +78,10 @@ constexpr int kBM = 128;  // query rows per Q tile (= TMEM lanes)
 constexpr int kBN = 128;  // keys per K/V block
 constexpr float kRescaleThreshold = 8.0f;
 
+#ifndef ATTN_FP8_POLY_QUADS
+#define ATTN_FP8_POLY_QUADS 0
+#endif
+
 template <int D, int KIND>
 struct Cfg {
   static constexpr int ELEM = KIND == KIND_E4M3 ? 1 : 2;  // operand bytes
@@ -91,6 +96,10 @@ struct Cfg {
   static constexpr int PV_STEPS = kBN / KSTEP;
   static constexpr int P_COLS = kBN * ELEM / 4;  // TMEM columns holding one row of P
   static constexpr int STAGES = KIND == KIND_E4M3 ? 8 : (D == 64 ? 6 : (D == 128 ? 4 : 2));
+  // E4M3 weights: quadruples out of every 8 (32 keys) whose 2^x runs on the
+  // FMA pipe instead of the multi-function unit (unmasked blocks only).
+  static constexpr int POLY_QUADS = KIND == KIND_E4M3 ? ATTN_FP8_POLY_QUADS : 0;
+  static_assert(POLY_QUADS >= 0 && POLY_QUADS <= 8, "quadruples per 32-key chunk");
   // Two Q tiles: the stages form pairs, one per key-block step j holding K_j
   // and V_{j-1} (consumed and released together), with one full and one
   // empty barrier per pair.  One Q tile: single-tile stages.
@@ -534,8 +543,11 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
       if constexpr (F8) {
         const int sb = w.bh * p.scale_bh_stride;
         c_q = p.sl2 * p.q_scale[sb + (tile_row0 / kBM) * p.scale_blk_stride];
+        // The lanes share the nb scale loads, then reduce across the warp.
         float mx = 0.f;
-        for (int j = 0; j < nb; ++j) mx = fmaxf(mx, p.v_scale[sb + j * p.scale_blk_stride]);
+        for (int j = lane; j < nb; j += 32) mx = fmaxf(mx, p.v_scale[sb + j * p.scale_blk_stride]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         sv_max = mx > 0.f ? mx : 1.f;
       }
 
@@ -638,25 +650,42 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
           rowsum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
         } else {
           // E4M3 weights, four per TMEM column; each 32-column chunk is stored
-          // as soon as it is packed.
+          // as soon as it is packed.  In blocks without masked keys the last
+          // POLY_QUADS quadruples of every chunk take 2^x on the FMA pipe
+          // (exp2_poly2), the rest on the multi-function unit, whose rate
+          // the weights of both Q tiles otherwise share; masked blocks take
+          // every weight from ex2.approx, which gives masked keys exact zeros.
           float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
           const float2 c2 = masked ? make_float2(1.f, 1.f) : make_float2(cj, cj);
           const float2 m2 = make_float2(neg_m, neg_m);
+          auto weights = [&](auto poly) {
+            constexpr bool kPoly = decltype(poly)::value;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t pk[8];
+            for (int c = 0; c < 4; ++c) {
+              uint32_t pk[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float2 a = ffma2(make_float2(__uint_as_float(s[c][4 * i]), __uint_as_float(s[c][4 * i + 1])), c2, m2);
-              const float2 bq = ffma2(make_float2(__uint_as_float(s[c][4 * i + 2]), __uint_as_float(s[c][4 * i + 3])), c2, m2);
-              const float2 p01 = make_float2(ex2(a.x), ex2(a.y));
-              const float2 p23 = make_float2(ex2(bq.x), ex2(bq.y));
-              acc0 = fadd2(acc0, p01);
-              acc1 = fadd2(acc1, p23);
-              pk[i] = pack4_e4m3(p01.x, p01.y, p23.x, p23.y);
+              for (int i = 0; i < 8; ++i) {
+                const float2 a = ffma2(make_float2(__uint_as_float(s[c][4 * i]), __uint_as_float(s[c][4 * i + 1])), c2, m2);
+                const float2 bq = ffma2(make_float2(__uint_as_float(s[c][4 * i + 2]), __uint_as_float(s[c][4 * i + 3])), c2, m2);
+                float2 p01, p23;
+                if (kPoly && i >= 8 - C::POLY_QUADS) {
+                  p01 = exp2_poly2(a);
+                  p23 = exp2_poly2(bq);
+                } else {
+                  p01 = make_float2(ex2(a.x), ex2(a.y));
+                  p23 = make_float2(ex2(bq.x), ex2(bq.y));
+                }
+                acc0 = fadd2(acc0, p01);
+                acc1 = fadd2(acc1, p23);
+                pk[i] = pack4_e4m3(p01.x, p01.y, p23.x, p23.y);
+              }
+              tmem_st8(tm_s + 8 * c, pk);
             }
-            tmem_st8(tm_s + 8 * c, pk);
-          }
+          };
+          if (masked || C::POLY_QUADS == 0)
+            weights(std::false_type{});
+          else
+            weights(std::true_type{});
           rowsum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
         }
 

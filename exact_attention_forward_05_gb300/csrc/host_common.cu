@@ -3,7 +3,10 @@
 #include "host_common.h"
 
 #include <atomic>
+#include <cstring>
 #include <mutex>
+
+#include "tmap_cache.h"
 
 namespace attn_internal {
 
@@ -58,9 +61,22 @@ int sm_count() {
   return n;
 }
 
+namespace {
+// 32 recent maps (a launch encodes four).
+TmapCache<CUtensorMap, 32> g_tmaps;
+}  // namespace
+
 bool encode_tmap_4d(CUtensorMap* out, CUtensorMapDataType dtype, const void* base,
                     const uint64_t (&dims)[4], const uint64_t (&strides)[3], const uint32_t (&box)[4],
                     CUtensorMapSwizzle swizzle) {
+  TmapKey key;
+  std::memset(&key, 0, sizeof(key));
+  key.base = reinterpret_cast<uint64_t>(base);
+  for (int i = 0; i < 4; ++i) key.dims[i] = dims[i], key.box[i] = box[i];
+  for (int i = 0; i < 3; ++i) key.strides[i] = strides[i];
+  key.dtype = static_cast<uint32_t>(dtype);
+  key.swizzle = static_cast<uint32_t>(swizzle);
+  if (g_tmaps.find(key, out)) return true;
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t gdims[4] = {dims[0], dims[1], dims[2], dims[3]};
@@ -70,7 +86,9 @@ bool encode_tmap_4d(CUtensorMap* out, CUtensorMapDataType dtype, const void* bas
   CUresult r = fn(out, dtype, 4, const_cast<void*>(base), gdims, gstrides, gbox, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) return false;
+  g_tmaps.insert(key, *out);
+  return true;
 }
 
 }  // namespace attn_internal

@@ -171,6 +171,15 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Untiled bulk copy global -> shared of `bytes` bytes (a multiple of 16; both
+// addresses 16-byte aligned), completing as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // 4-D tiled store from shared memory (bulk-group completion); elements of the
 // box outside the tensor are not written.
 __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t src, int x, int y, int z,
@@ -384,10 +393,49 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
       "l"(*reinterpret_cast<unsigned long long*>(&b)));
   return *reinterpret_cast<float2*>(&d);
 }
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(*reinterpret_cast<unsigned long long*>(&a)),
+      "l"(*reinterpret_cast<unsigned long long*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(*reinterpret_cast<unsigned long long*>(&a)),
+      "l"(*reinterpret_cast<unsigned long long*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
+}
 __device__ __forceinline__ float min3(float a, float b, float c) {
   float d;
   asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
+}
+
+// 2^x of two values on the FMA pipe, for x <= 127, as a stand-in for
+// ex2.approx that leaves the multi-function unit to other work (Cody-Waite
+// style range reduction):
+//   x is clamped to >= -125, so that 2^n below stays a normal float (2^x is
+//   then at least 2^-125.5 instead of smaller or zero);
+//   n = round(x) from the low mantissa bits of t = x + 1.5 * 2^23 (exact for
+//   |x| < 2^22), f = x - n in [-1/2, 1/2], exact;
+//   2^f by a cubic of our own fit (Remez exchange on the relative error over
+//   [-1/2, 1/2]): maximum relative error 7.5e-5 in float32 Horner form;
+//   2^n applied by an integer add of n << 23 into the exponent field, which
+//   is (bits(t) << 23) since the magic constant's low 9 bits are zero.
+constexpr float kExp2Magic = 12582912.0f;  // 1.5 * 2^23
+constexpr float kExp2C0 = 0.99992807f, kExp2C1 = 0.69326099f, kExp2C2 = 0.24261112f,
+                kExp2C3 = 0.05517167f;
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+  x.x = fmaxf(x.x, -125.f);
+  x.y = fmaxf(x.y, -125.f);
+  const float2 magic = make_float2(kExp2Magic, kExp2Magic);
+  const float2 t = fadd2(x, magic);
+  const float2 f = fsub2(x, fsub2(t, magic));
+  float2 p = ffma2(f, make_float2(kExp2C3, kExp2C3), make_float2(kExp2C2, kExp2C2));
+  p = ffma2(p, f, make_float2(kExp2C1, kExp2C1));
+  p = ffma2(p, f, make_float2(kExp2C0, kExp2C0));
+  return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
+                     __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
 }
 
 }  // namespace sm103

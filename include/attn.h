@@ -23,8 +23,11 @@
  *    queries and keys of different lengths (Nq, Nk).
  *  - Device pointers are CUDA device addresses on the current device; every
  *    tensor base must be 16-byte aligned (lse: 4-byte aligned).
- *  - Ownership: the caller owns every buffer.  The library never allocates
- *    device memory; it keeps one device status word per kernel module.
+ *  - Ownership: the caller owns every buffer.  The library allocates no device
+ *    memory per call.  It keeps one device status word per kernel module and,
+ *    as the one exception, a fixed 64 MiB array in its own device memory that
+ *    serves only attn_fwd_host_noalloc (resident on every device that loads
+ *    the library, until the process exits).
  *  - Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  All
  *    device-pointer entry points are asynchronous on that stream.
  *  - Errors: arguments are validated before anything is launched; a bad
@@ -159,7 +162,11 @@ attn_status attn_fwd_host(const void* q_host, const void* k_host, const void* v_
  *    contents; nothing in it has to start at zero (each call writes every byte
  *    it reads).  Calls whose GPU work overlaps (other host threads or streams
  *    at the same time) race on the array and must not be issued.
- * Other arguments, copies and synchronisation as for attn_fwd_host.
+ * Other arguments, copies and synchronisation as for attn_fwd_host.  As there,
+ * ATTN_OK means the copies and the kernel ran to completion on the GPU, but a
+ * kernel whose internal wait ran past its limit stops early and leaves O and
+ * lse unfinished while the call still returns ATTN_OK: follow a successful
+ * call with attn_get_device_status() to rule that out.
  */
 #define ATTN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 attn_status attn_fwd_host_noalloc(const void* q_host, const void* k_host, const void* v_host,
@@ -221,12 +228,17 @@ attn_status attn_fp8_prepare_rotary(const void* q, const void* k, const void* v,
 
 /*
  * attn_fwd_fp8 -- exact attention forward on E4M3 operands with float32 scales
- * (as written by attn_fp8_prepare), bf16 output.
+ * (as written by attn_fp8_prepare), bf16 output.  The FP8 tensor-core path of
+ * "New GPU Features on Hopper: WGMMA, TMA, FP8" (FlashAttention-3 podcast
+ * page), on the block-quantised operands of item 3 of "Метод" in the
+ * comrad404 review.
  *
  *   q8, k8, v8 : [B, H, N, d] device E4M3 codes, read only; the true values are
  *                code * scale of their 128-row block (or of the tensor).
  *   q_scale, k_scale, v_scale : device float32, layout as for attn_fp8_prepare.
- *   per_tensor : 1 if the scales are single per-tensor values.
+ *   per_tensor : 1 if the scales are single per-tensor values.  This argument
+ *                widens the planned interface: it lets the same kernel run
+ *                the naive per-tensor FP8 baseline the pages compare against.
  *   o          : [B, H, N, d] device bf16, written.
  *   lse        : [B, H, N] device float32 or NULL.
  *   d          : 128.  Other arguments as for attn_fwd.
@@ -277,6 +289,29 @@ attn_status attn_set_schedule(int mode);
  * ATTN_ERR_TIMEOUT.  Asynchronous on `stream`.
  */
 attn_status attn_debug_bounded_wait(uint64_t timeout_ns, void* stream);
+
+/*
+ * attn_debug_fail_host_chunk -- test hook for the error path of the host-buffer
+ * entry points.  Arms a one-shot failure: the next attn_fwd_host (or
+ * attn_fwd_host_noalloc) call enqueues the copies of its pipeline chunk
+ * `chunk` and then, in place of that chunk's kernel launch, returns
+ * ATTN_ERR_CUDA as if the launch had failed, after waiting for everything it
+ * had already enqueued.  Nothing faults on the device.  A negative `chunk`
+ * disarms the hook; a chunk index past the call's last chunk never fires and
+ * is cleared by that call.
+ */
+void attn_debug_fail_host_chunk(int chunk);
+
+/*
+ * attn_debug_exp2_poly -- test hook for the polynomial 2^x that part of the FP8
+ * softmax weights use on the FMA pipe instead of ex2.approx (a cubic after
+ * rounding the argument to the nearest integer, with the argument clamped to
+ * >= -125; relative error below 7.6e-5 for -125 <= x <= 127).  For n float32
+ * values x (device), writes that function to y_poly and CUDA's exp2f to y_ref
+ * (device, n floats each).  Asynchronous on `stream`.  ATTN_ERR_INVALID_ARG
+ * for n < 0 or a NULL pointer when n > 0.
+ */
+attn_status attn_debug_exp2_poly(const float* x, float* y_poly, float* y_ref, int n, void* stream);
 
 /* Last CUDA error code seen by the library (cudaError_t as int; 0 = none). */
 int attn_last_cuda_error(void);
