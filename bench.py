@@ -722,14 +722,18 @@ def run_sweep(args):
                          lambda: attn.attn_fwd(q, k, v, causal=causal, scale=d ** -0.5, out=o, lse=lse,
                                                stream=stream))
                 del q, k, v, o, lse
-            B, H, d = 16384 // N, 16, 128
-            q, k, v = (t.to(dev) for t in synth.outlier_inputs(B, H, N, d, "bf16", seed=0))
-            bufs = attn.fp8_prepare(q, k, v, signs=synth.hadamard_signs(H, d, seed=0).to(dev))
-            o8 = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
-            for causal in (False, True):
-                emit(dict(B=B, H=H, N=N, d=d, causal=causal, dtype="fp8 e4m3"),
-                     lambda: attn.attn_fwd_fp8(*bufs, causal=causal, scale=d ** -0.5, out=o8,
-                                               return_lse=False, stream=stream), fp8=True)
+            # FP8: d = 128 with H = 16 (the FP8 workload), d = 64 and 256 with the
+            # bf16 sweep's H = 2048 / d.
+            for d in (64, 128, 256):
+                B, H = 16384 // N, (16 if d == 128 else 2048 // d)
+                q, k, v = (t.to(dev) for t in synth.outlier_inputs(B, H, N, d, "bf16", seed=0))
+                bufs = attn.fp8_prepare(q, k, v, signs=synth.hadamard_signs(H, d, seed=0).to(dev))
+                o8 = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+                for causal in (False, True):
+                    emit(dict(B=B, H=H, N=N, d=d, causal=causal, dtype="fp8 e4m3"),
+                         lambda: attn.attn_fwd_fp8(*bufs, causal=causal, scale=d ** -0.5, out=o8,
+                                                   return_lse=False, stream=stream), fp8=True)
+                del q, k, v, bufs, o8
         # Long-context configuration: B = 1, H = 16, N = 32768, d = 128, causal.
         B, H, N, d = 1, 16, 32768, 128
         q, k, v = (t.to(dev) for t in synth.attention_inputs(B, H, N, d, "bf16", seed=0))

@@ -2,7 +2,7 @@
 //
 // Pre-pass ("Incoherent Processing for FP8 Accuracy", FlashAttention-3 podcast
 // page; comrad404 review, "Метод", item 3): every row of Q and K is multiplied
-// by diag(sigma_h) H_128 / sqrt(128) -- random signs of its head, then the
+// by diag(sigma_h) H_d / sqrt(d) -- random signs of its head, then the
 // Sylvester Hadamard transform, O(d log d) butterflies -- and Q, K, V are
 // quantised to E4M3 with one float32 scale per 128 rows of a head:
 // s = amax / 448 (1 when the block is all zero), code = RNE_satfinite(x / s).
@@ -16,7 +16,8 @@
 // (2i, 2i+1) or (i, i + d/2)), in the registers that then take the rotation,
 // so the fused step reads and writes each row once.
 //
-// The attention kernel itself is attn_kernel::attn_fwd_kernel<128, E4M3>.
+// The pre-pass takes d = 64, 128 or 256; the attention kernel itself is
+// attn_kernel::attn_fwd_kernel<d, E4M3>.
 #include "attn_kernel.cuh"
 
 using attn_kernel::FwdParams;
@@ -28,9 +29,10 @@ using sm103::fsub2;
 
 namespace {
 
-constexpr int kHeadDim = 128;     // FP8 path: d = 128
+using namespace sm103;
+
 constexpr int kQuantRows = 128;   // rows per scale block
-constexpr int kPrepThreads = 512; // 16 warps x 8 rows, 4 lanes x 32 values per row
+constexpr int kPrepThreads = 512; // 128 rows x 4 lanes; a lane holds d / 4 values of its row
 constexpr float kE4M3Max = 448.0f;
 
 enum PrepMode : int { PREP_BLOCK = 0, PREP_AMAX = 1, PREP_QUANT_GLOBAL = 2 };
@@ -39,52 +41,12 @@ struct PrepParams {
   const void* src[3];
   uint8_t* dst[3];
   float* scale[3];
-  const int8_t* signs;  // [H][128] +-1, or nullptr (no rotation)
-  const float* rcos;    // [N][64] rotary tables, or nullptr (no rotary embedding)
+  const int8_t* signs;  // [H][d] +-1, or nullptr (no rotation)
+  const float* rcos;    // [N][d/2] rotary tables, or nullptr (no rotary embedding)
   const float* rsin;
-  int rope_interleaved; // pairs (2i, 2i+1) if nonzero, else (i, i + 64)
-  int H, N, nblk;
+  int rope_interleaved; // pairs (2i, 2i+1) if nonzero, else (i, i + d/2)
+  int H, N, nblk, BH;
 };
-
-__device__ __forceinline__ float2 pair(const float (&x)[32], int e) { return make_float2(x[e], x[e + 1]); }
-__device__ __forceinline__ void put(float (&x)[32], int e, float2 v) {
-  x[e] = v.x;
-  x[e + 1] = v.y;
-}
-
-// Sylvester-ordered fast Walsh-Hadamard transform of one 128-element row held
-// by 4 lanes (lane g of the group owns elements 32 g .. 32 g + 31): butterflies
-// of stride 1 .. 16 inside the thread, 32 and 64 across the group.  The stages
-// commute, so any order gives the transform.  Strides 2 .. 16 and the lane
-// stages combine whole element pairs with paired instructions.
-__device__ __forceinline__ void fwht128(float (&x)[32], int g) {
-#pragma unroll
-  for (int e = 0; e < 32; e += 2) {
-    const float a = x[e], b = x[e + 1];
-    x[e] = a + b;
-    x[e + 1] = a - b;
-  }
-#pragma unroll
-  for (int m = 2; m < 32; m <<= 1)
-#pragma unroll
-    for (int e = 0; e < 32; e += 2)
-      if ((e & m) == 0) {
-        const float2 a = pair(x, e), b = pair(x, e + m);
-        put(x, e, fadd2(a, b));
-        put(x, e + m, fsub2(a, b));
-      }
-#pragma unroll
-  for (int m = 1; m < 4; m <<= 1) {
-    const float sgn = (g & m) ? -1.f : 1.f;  // upper half of the pair: partner - own
-    const float2 sg2 = make_float2(sgn, sgn);
-#pragma unroll
-    for (int e = 0; e < 32; e += 2) {
-      const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, x[e], m),
-                                   __shfl_xor_sync(0xffffffffu, x[e + 1], m));
-      put(x, e, ffma2(pair(x, e), sg2, o));
-    }
-  }
-}
 
 // Correctly rounded x / s from y = RN(1 / s) with one FMA correction of the
 // product (Markstein, "Computation of elementary functions on the IBM RISC
@@ -98,15 +60,113 @@ __device__ __forceinline__ float2 div_by_scale2(float2 x, float2 ns2, float2 y2)
   return ffma2(r, y2, q0);
 }
 
-template <bool BF16IN, int MODE>
-__global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const PrepParams p) {
+template <int VPL>
+__device__ __forceinline__ float2 pair(const float (&x)[VPL], int e) { return make_float2(x[e], x[e + 1]); }
+template <int VPL>
+__device__ __forceinline__ void put(float (&x)[VPL], int e, float2 v) {
+  x[e] = v.x;
+  x[e + 1] = v.y;
+}
+
+// Sylvester-ordered fast Walsh-Hadamard transform of one row of 4 * VPL
+// elements held by the 4 lanes of its group (lane g owns elements
+// VPL g .. VPL g + VPL - 1): butterflies of stride 1 .. VPL / 2 inside the
+// thread, VPL and 2 VPL across the group.  The stages commute, so any order
+// gives the transform.  Strides from 2 on combine whole element pairs with
+// paired instructions.
+template <int VPL>
+__device__ __forceinline__ void fwht_row(float (&x)[VPL], int g) {
+#pragma unroll
+  for (int e = 0; e < VPL; e += 2) {
+    const float a = x[e], b = x[e + 1];
+    x[e] = a + b;
+    x[e + 1] = a - b;
+  }
+#pragma unroll
+  for (int m = 2; m < VPL; m <<= 1)
+#pragma unroll
+    for (int e = 0; e < VPL; e += 2)
+      if ((e & m) == 0) {
+        const float2 a = pair(x, e), b = pair(x, e + m);
+        put(x, e, fadd2(a, b));
+        put(x, e + m, fsub2(a, b));
+      }
+#pragma unroll
+  for (int m = 1; m < 4; m <<= 1) {
+    const float sgn = (g & m) ? -1.f : 1.f;  // upper half of the pair: partner - own
+    const float2 sg2 = make_float2(sgn, sgn);
+#pragma unroll
+    for (int e = 0; e < VPL; e += 2) {
+      const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, x[e], m),
+                                   __shfl_xor_sync(0xffffffffu, x[e + 1], m));
+      put(x, e, ffma2(pair(x, e), sg2, o));
+    }
+  }
+}
+
+// Rotary embedding of this lane's VPL values of a row: (a, b) -> (a cos - b sin,
+// a sin + b cos), table entries from `cr` / `sr` (the row's d/2 cos and sin
+// values, shared or global memory).  Interleaved pairs (2i, 2i+1) are inside
+// the lane; half-split pairs (i, i + d/2) pair lane g with lane g ^ 2 of the
+// row's group, one shuffle per value (every lane of the warp takes part).
+template <int VPL>
+__device__ __forceinline__ void rotary_row(float (&x)[VPL], int g, const float* cr, const float* sr,
+                                           bool interleaved, bool have) {
+  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (interleaved) {
+    // This lane's elements VPL g .. are the pairs i = VPL g / 2 ...
+    const float4* c4 = reinterpret_cast<const float4*>(cr + (VPL / 2) * g);
+    const float4* s4 = reinterpret_cast<const float4*>(sr + (VPL / 2) * g);
+#pragma unroll
+    for (int w = 0; w < VPL / 8; ++w) {
+      const float4 cv = have ? c4[w] : zero4, sv = have ? s4[w] : zero4;
+      const float cc[4] = {cv.x, cv.y, cv.z, cv.w}, ss[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = 8 * w + 2 * u;
+        const float a = x[e], b = x[e + 1];
+        // (a c - b s, a s + b c): b (-s, c), then a (c, s) added with one rounding.
+        const float2 t2 = fmul2(make_float2(b, b), make_float2(-ss[u], cc[u]));
+        put(x, e, ffma2(make_float2(a, a), make_float2(cc[u], ss[u]), t2));
+      }
+    }
+  } else {
+    // Pair i = VPL (g & 1) + e is (element i, element i + d/2): lanes g and g ^ 2
+    // of the row's group hold its two halves.
+    const float4* c4 = reinterpret_cast<const float4*>(cr + VPL * (g & 1));
+    const float4* s4 = reinterpret_cast<const float4*>(sr + VPL * (g & 1));
+    const float sgn = (g & 2) ? 1.f : -1.f;  // second half: b cos + a sin
+#pragma unroll
+    for (int w = 0; w < VPL / 4; ++w) {
+      const float4 cv = have ? c4[w] : zero4, sv = have ? s4[w] : zero4;
+      const float cc[4] = {cv.x, cv.y, cv.z, cv.w}, ss[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+      for (int u = 0; u < 4; u += 2) {
+        const int e = 4 * w + u;
+        const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, x[e], 2),
+                                     __shfl_xor_sync(0xffffffffu, x[e + 1], 2));
+        const float2 t2 = fmul2(pair(x, e), make_float2(cc[u], cc[u + 1]));
+        put(x, e, ffma2(o, make_float2(sgn * ss[u], sgn * ss[u + 1]), t2));
+      }
+    }
+  }
+}
+
+// One CTA of 512 threads per (128-row block, tensor, head) item; two CTAs
+// share an SM at d <= 128.  Every lane loads its d / 4 values of its row
+// (row-contiguous 16-byte loads), applies the rotary embedding, the signs and
+// the Hadamard transform (Q and K), the block maximum is reduced across the
+// CTA, and the lane quantises and stores its codes.
+template <int D, bool BF16IN, int MODE>
+__global__ void __launch_bounds__(kPrepThreads, D <= 128 ? 2 : 1) fp8_prepare_kernel(const PrepParams p) {
+  constexpr int VPL = D / 4;
   const int t = blockIdx.y;                     // 0 = Q, 1 = K, 2 = V
   const int blk = blockIdx.x % p.nblk;
   const int bh = blockIdx.x / p.nblk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane & 3;                       // lane within the row's group of 4
-  const bool rotate = t < 2 && p.signs != nullptr;
-  const size_t head = static_cast<size_t>(bh) * p.N * kHeadDim;
+  const bool qk = t < 2;
+  const size_t head = static_cast<size_t>(bh) * p.N * D;
   // Operands chosen by selects, not by indexing the parameter arrays (which
   // would copy them to local memory).
   const uint8_t* src = static_cast<const uint8_t*>(t == 0 ? p.src[0] : t == 1 ? p.src[1] : p.src[2]);
@@ -114,97 +174,60 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const PrepPar
   uint8_t* dst = t == 0 ? p.dst[0] : t == 1 ? p.dst[1] : p.dst[2];
 
   const int row = blk * kQuantRows + warp * 8 + (lane >> 2);
-  float x[32];
-  if (row < p.N) {
-    const uint4* ptr = reinterpret_cast<const uint4*>(
-        src + (head + static_cast<size_t>(row) * kHeadDim + 32 * g) * 2);
+  const bool have = row < p.N;
+  float x[VPL];
+  if (have) {
+    const uint4* ptr = reinterpret_cast<const uint4*>(src + (head + static_cast<size_t>(row) * D + VPL * g) * 2);
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
+    for (int v = 0; v < VPL / 8; ++v) {
       const uint4 r = ptr[v];
-      const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+      const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         float2 f;
-        if constexpr (BF16IN) f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
-        else f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+        if constexpr (BF16IN) f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[k]));
+        else f = __half22float2(*reinterpret_cast<const __half2*>(&w4[k]));
         x[8 * v + 2 * k] = f.x;
         x[8 * v + 2 * k + 1] = f.y;
       }
     }
   } else {
 #pragma unroll
-    for (int e = 0; e < 32; ++e) x[e] = 0.f;
+    for (int e = 0; e < VPL; ++e) x[e] = 0.f;
   }
-  if (t < 2 && p.rcos != nullptr) {
-    // Rotary embedding: (a, b) -> (a cos - b sin, a sin + b cos).  Block-uniform
-    // branch (the half-split form shuffles); rows past N are zero and skip the
-    // table loads.
-    const bool have = row < p.N;
-    const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float* cr = p.rcos + static_cast<size_t>(have ? row : 0) * (kHeadDim / 2);
-    const float* sr = p.rsin + static_cast<size_t>(have ? row : 0) * (kHeadDim / 2);
-    if (p.rope_interleaved) {
-      // This lane's elements 32 g .. 32 g + 31 are the pairs i = 16 g .. 16 g + 15.
-      const float4* c4 = reinterpret_cast<const float4*>(cr + 16 * g);
-      const float4* s4 = reinterpret_cast<const float4*>(sr + 16 * g);
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const float4 cv = have ? c4[w] : zero4, sv = have ? s4[w] : zero4;
-        const float cc[4] = {cv.x, cv.y, cv.z, cv.w}, ss[4] = {sv.x, sv.y, sv.z, sv.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int e = 8 * w + 2 * u;
-          const float a = x[e], b = x[e + 1];
-          // (a c - b s, a s + b c): b (-s, c), then a (c, s) added with one rounding.
-          const float2 t2 = fmul2(make_float2(b, b), make_float2(-ss[u], cc[u]));
-          put(x, e, ffma2(make_float2(a, a), make_float2(cc[u], ss[u]), t2));
-        }
-      }
-    } else {
-      // Pair i = 32 (g & 1) + e is (element i, element i + 64): lanes g and g ^ 2
-      // of the row's group hold its two halves.
-      const float4* c4 = reinterpret_cast<const float4*>(cr + 32 * (g & 1));
-      const float4* s4 = reinterpret_cast<const float4*>(sr + 32 * (g & 1));
-      const float sgn = (g & 2) ? 1.f : -1.f;  // second half: b cos + a sin
-#pragma unroll
-      for (int w = 0; w < 8; ++w) {
-        const float4 cv = have ? c4[w] : zero4, sv = have ? s4[w] : zero4;
-        const float cc[4] = {cv.x, cv.y, cv.z, cv.w}, ss[4] = {sv.x, sv.y, sv.z, sv.w};
-#pragma unroll
-        for (int u = 0; u < 4; u += 2) {
-          const int e = 4 * w + u;
-          const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, x[e], 2),
-                                       __shfl_xor_sync(0xffffffffu, x[e + 1], 2));
-          const float2 t2 = fmul2(pair(x, e), make_float2(cc[u], cc[u + 1]));
-          put(x, e, ffma2(o, make_float2(sgn * ss[u], sgn * ss[u + 1]), t2));
-        }
-      }
-    }
+  if (qk && p.rcos != nullptr) {
+    // Block-uniform branch (the half-split form shuffles); rows past N are
+    // zero and skip the table loads.
+    const float* cr = p.rcos + static_cast<size_t>(have ? row : 0) * (D / 2);
+    const float* sr = p.rsin + static_cast<size_t>(have ? row : 0) * (D / 2);
+    rotary_row<VPL>(x, g, cr, sr, p.rope_interleaved != 0, have);
   }
-  if (rotate) {
+  if (qk && p.signs != nullptr) {
     // Signs (+1 = 0x01, -1 = 0xff): bit 7 of each byte becomes the float's sign bit.
-    const int4* sp = reinterpret_cast<const int4*>(p.signs + (bh % p.H) * kHeadDim + 32 * g);
-    const int4 s0 = sp[0], s1 = sp[1];
-    const uint32_t sw[8] = {static_cast<uint32_t>(s0.x), static_cast<uint32_t>(s0.y),
-                            static_cast<uint32_t>(s0.z), static_cast<uint32_t>(s0.w),
-                            static_cast<uint32_t>(s1.x), static_cast<uint32_t>(s1.y),
-                            static_cast<uint32_t>(s1.z), static_cast<uint32_t>(s1.w)};
+    const int4* sp = reinterpret_cast<const int4*>(p.signs + (bh % p.H) * D + VPL * g);
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const uint32_t bit = (sw[e >> 2] << (24 - 8 * (e & 3))) & 0x80000000u;
-      x[e] = __uint_as_float(__float_as_uint(x[e]) ^ bit);
+    for (int v = 0; v < VPL / 16; ++v) {
+      const int4 sv = sp[v];
+      const uint32_t sw[4] = {static_cast<uint32_t>(sv.x), static_cast<uint32_t>(sv.y),
+                              static_cast<uint32_t>(sv.z), static_cast<uint32_t>(sv.w)};
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const uint32_t bit = (sw[e >> 2] << (24 - 8 * (e & 3))) & 0x80000000u;
+        x[16 * v + e] = __uint_as_float(__float_as_uint(x[16 * v + e]) ^ bit);
+      }
     }
-    fwht128(x, g);
-    const float2 inv_sqrt_d = make_float2(0.08838834764831845f, 0.08838834764831845f);  // 1 / sqrt(128)
+    fwht_row<VPL>(x, g);
+    constexpr float inv_sqrt_d = D == 64 ? 0.125f : (D == 128 ? 0.08838834764831845f : 0.0625f);
+    const float2 isd = make_float2(inv_sqrt_d, inv_sqrt_d);
 #pragma unroll
-    for (int e = 0; e < 32; e += 2) put(x, e, fmul2(pair(x, e), inv_sqrt_d));
+    for (int e = 0; e < VPL; e += 2) put(x, e, fmul2(pair(x, e), isd));
   }
 
   // amax of the block
   __shared__ float warp_max[kPrepThreads / 32];
   float a = 0.f;
 #pragma unroll
-  for (int e = 0; e < 32; ++e) a = fmaxf(a, fabsf(x[e]));
+  for (int e = 0; e < VPL; e += 2) a = max3(a, fabsf(x[e]), fabsf(x[e + 1]));
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
   if (lane == 0) warp_max[warp] = a;
@@ -228,11 +251,11 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const PrepPar
     // Block-uniform choice: the FMA-corrected quotient for ordinary scales.
     const bool fast = s >= 0x1p-100f && s <= 0x1p+100f;
     const float y = __frcp_rn(s);
-    if (row < p.N) {
-      uint32_t pk[8];
+    if (have) {
+      uint32_t pk[VPL / 4];
       const float2 ns2 = make_float2(-s, -s), y2 = make_float2(y, y);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < VPL / 4; ++k) {
         float2 q01, q23;
         if (fast) {
           q01 = div_by_scale2(pair(x, 4 * k), ns2, y2);
@@ -245,9 +268,9 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const PrepPar
         const uint32_t hi = __nv_cvt_float2_to_fp8x2(q23, __NV_SATFINITE, __NV_E4M3);
         pk[k] = lo | (hi << 16);
       }
-      uint4* out = reinterpret_cast<uint4*>(dst + head + static_cast<size_t>(row) * kHeadDim + 32 * g);
-      out[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      out[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      uint4* out = reinterpret_cast<uint4*>(dst + head + static_cast<size_t>(row) * D + VPL * g);
+#pragma unroll
+      for (int v = 0; v < VPL / 16; ++v) out[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
     }
   }
 }
@@ -261,26 +284,38 @@ __global__ void fp8_finalize_scale_kernel(float* q_scale, float* k_scale, float*
   }
 }
 
-template <bool BF16IN>
-attn_status run_prepare(const PrepParams& prm, int BH, int per_tensor, cudaStream_t s) {
-  const dim3 grid(static_cast<unsigned>(BH) * prm.nblk, 3);
+template <int D, bool BF16IN>
+attn_status run_prepare_d(const PrepParams& prm, int per_tensor, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>(prm.BH) * prm.nblk, 3);
   if (!per_tensor) {
-    fp8_prepare_kernel<BF16IN, PREP_BLOCK><<<grid, kPrepThreads, 0, s>>>(prm);
+    fp8_prepare_kernel<D, BF16IN, PREP_BLOCK><<<grid, kPrepThreads, 0, s>>>(prm);
     return attn_internal::cuda_status(cudaGetLastError());
   }
   for (int t = 0; t < 3; ++t) {
     cudaError_t e = cudaMemsetAsync(prm.scale[t], 0, sizeof(float), s);
     if (e != cudaSuccess) return attn_internal::cuda_status(e);
   }
-  fp8_prepare_kernel<BF16IN, PREP_AMAX><<<grid, kPrepThreads, 0, s>>>(prm);
-  fp8_prepare_kernel<BF16IN, PREP_QUANT_GLOBAL><<<grid, kPrepThreads, 0, s>>>(prm);
+  fp8_prepare_kernel<D, BF16IN, PREP_AMAX><<<grid, kPrepThreads, 0, s>>>(prm);
+  fp8_prepare_kernel<D, BF16IN, PREP_QUANT_GLOBAL><<<grid, kPrepThreads, 0, s>>>(prm);
   fp8_finalize_scale_kernel<<<1, 32, 0, s>>>(prm.scale[0], prm.scale[1], prm.scale[2]);
   return attn_internal::cuda_status(cudaGetLastError());
 }
 
-attn_status check_common(int B, int H, int N, int d) {
+template <bool BF16IN>
+attn_status run_prepare(const PrepParams& prm, int d, int per_tensor, cudaStream_t s) {
+  switch (d) {
+    case 64: return run_prepare_d<64, BF16IN>(prm, per_tensor, s);
+    case 128: return run_prepare_d<128, BF16IN>(prm, per_tensor, s);
+    default: return run_prepare_d<256, BF16IN>(prm, per_tensor, s);
+  }
+}
+
+// Head dimensions of the FP8 pre-pass, and of the FP8 attention kernel.
+bool prep_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
+bool fwd_fp8_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
+
+attn_status check_common(int B, int H, int N) {
   if (B < 0 || H < 0 || N < 0) return ATTN_ERR_INVALID_ARG;
-  if (d != kHeadDim) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(B) * H > 0x7fffffff / 64) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
@@ -297,9 +332,11 @@ ATTN_EXPORT attn_status attn_fp8_prepare_rotary(const void* q, const void* k, co
                                                 const int8_t* signs, int per_tensor, const float* rope_cos,
                                                 const float* rope_sin, int rope_interleaved, int B, int H,
                                                 int N, int d, void* stream) {
-  attn_status st = check_common(B, H, N, d);
+  attn_status st = check_common(B, H, N);
   if (st != ATTN_OK) return st;
+  if (!prep_head_dim(d)) return ATTN_ERR_UNSUPPORTED;
   if (in_dtype != ATTN_FP16 && in_dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * H * ((N + kQuantRows - 1) / kQuantRows) > 0x7fffffff) return ATTN_ERR_INVALID_ARG;
   if ((rope_cos == nullptr) != (rope_sin == nullptr)) return ATTN_ERR_INVALID_ARG;
   if (static_cast<int64_t>(B) * H * N == 0) return ATTN_OK;
   if (!q || !k || !v || !q8 || !k8 || !v8 || !q_scale || !k_scale || !v_scale) return ATTN_ERR_INVALID_ARG;
@@ -323,10 +360,10 @@ ATTN_EXPORT attn_status attn_fp8_prepare_rotary(const void* q, const void* k, co
   prm.H = H;
   prm.N = N;
   prm.nblk = (N + kQuantRows - 1) / kQuantRows;
+  prm.BH = B * H;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int BH = B * H;
-  return in_dtype == ATTN_BF16 ? run_prepare<true>(prm, BH, per_tensor, s)
-                               : run_prepare<false>(prm, BH, per_tensor, s);
+  return in_dtype == ATTN_BF16 ? run_prepare<true>(prm, d, per_tensor, s)
+                               : run_prepare<false>(prm, d, per_tensor, s);
 }
 
 ATTN_EXPORT attn_status attn_fp8_prepare(const void* q, const void* k, const void* v, attn_dtype in_dtype,
@@ -341,8 +378,9 @@ ATTN_EXPORT attn_status attn_fwd_fp8(const void* q8, const void* k8, const void*
                                      const float* k_scale, const float* v_scale, int per_tensor, void* o,
                                      float* lse, int B, int H, int N, int d, int causal, float scale,
                                      void* stream) {
-  attn_status st = check_common(B, H, N, d);
+  attn_status st = check_common(B, H, N);
   if (st != ATTN_OK) return st;
+  if (!fwd_fp8_head_dim(d)) return ATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (static_cast<int64_t>(B) * H * N == 0) return ATTN_OK;
   if (!q8 || !k8 || !v8 || !o || !q_scale || !k_scale || !v_scale) return ATTN_ERR_INVALID_ARG;
@@ -360,6 +398,10 @@ ATTN_EXPORT attn_status attn_fwd_fp8(const void* q8, const void* k8, const void*
   const int nblk = (N + kQuantRows - 1) / kQuantRows;
   prm.scale_bh_stride = per_tensor ? 0 : nblk;
   prm.scale_blk_stride = per_tensor ? 0 : 1;
-  return attn_kernel::launch_fwd<kHeadDim, KIND_E4M3>(q8, k8, v8, prm, B, H, N, N, scale,
-                                                      static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  switch (d) {
+    case 64: return attn_kernel::launch_fwd<64, KIND_E4M3>(q8, k8, v8, prm, B, H, N, N, scale, s);
+    case 128: return attn_kernel::launch_fwd<128, KIND_E4M3>(q8, k8, v8, prm, B, H, N, N, scale, s);
+    default: return attn_kernel::launch_fwd<256, KIND_E4M3>(q8, k8, v8, prm, B, H, N, N, scale, s);
+  }
 }

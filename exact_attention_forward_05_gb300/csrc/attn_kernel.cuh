@@ -87,15 +87,19 @@ struct Cfg {
   static constexpr int ELEM = KIND == KIND_E4M3 ? 1 : 2;  // operand bytes
   static constexpr int NQ = D <= 128 ? 2 : 1;              // Q tiles per unit
   static constexpr int ROW_BYTES = D * ELEM;
-  static constexpr int CHUNK_BYTES = kBM * 128;  // 128 rows x one 128-byte swizzle span
-  static constexpr int CHUNK_ELEMS = 128 / ELEM;
-  static constexpr int CHUNKS = ROW_BYTES / 128;
+  // Swizzle span: 128 bytes, or 64 for the 64-byte rows of E4M3 at d = 64.
+  static constexpr int SW = ROW_BYTES >= 128 ? 128 : 64;
+  static constexpr int CHUNK_BYTES = kBM * SW;  // 128 rows x one swizzle span
+  static constexpr int CHUNK_ELEMS = SW / ELEM;
+  static constexpr int CHUNKS = ROW_BYTES / SW;
   static constexpr int TILE_BYTES = CHUNKS * CHUNK_BYTES;
+  static constexpr int K_PER_SPAN = SW / 32;     // MMA K steps (32 bytes each) per swizzle span
   static constexpr int KSTEP = 32 / ELEM;       // K elements per MMA instruction
   static constexpr int QK_STEPS = D / KSTEP;
   static constexpr int PV_STEPS = kBN / KSTEP;
   static constexpr int P_COLS = kBN * ELEM / 4;  // TMEM columns holding one row of P
-  static constexpr int STAGES = KIND == KIND_E4M3 ? 8 : (D == 64 ? 6 : (D == 128 ? 4 : 2));
+  static constexpr int STAGES = KIND == KIND_E4M3 ? (D == 64 ? 12 : (D == 128 ? 8 : 4))
+                                                 : (D == 64 ? 6 : (D == 128 ? 4 : 2));
   // E4M3 weights: quadruples out of every 8 (32 keys) whose 2^x runs on the
   // FMA pipe instead of the multi-function unit (unmasked blocks only).
   static constexpr int POLY_QUADS = KIND == KIND_E4M3 ? ATTN_FP8_POLY_QUADS : 0;
@@ -140,7 +144,7 @@ struct Cfg {
   static constexpr int SMEM_BYTES = OFF_BAR + 8 * NBARS + 16 + 1024;
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(SMEM_BYTES > 114 * 1024, "one CTA per SM (TMEM is allocated whole)");
-  static_assert(ROW_BYTES % 128 == 0, "rows span whole 128-byte swizzle spans");
+  static_assert(ROW_BYTES % SW == 0, "rows span whole swizzle spans");
 };
 
 struct FwdParams {
@@ -409,14 +413,15 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
       };
       // S[sbuf] = Q[qt] K^T   (K-major A and B, 128-byte swizzle; 32 bytes of K per MMA)
       // Descriptors: base low word once per call, a constant offset per product.
-      constexpr uint32_t DESC_HI = desc_sw128_hi(1024);
+      // 8-row groups of SW-byte rows: stride 8 * SW bytes.
+      constexpr uint32_t DESC_HI = C::SW == 128 ? desc_sw128_hi(1024) : desc_sw64_hi(512);
       auto issue_qk = [&](int qt, int sbuf, uint32_t kslot) {
         const uint32_t d_tmem = tmem + (sbuf ? C::TM_S1 : C::TM_S0);
         const uint32_t a0 = desc_sw128_lo(sQ + qt * C::TILE_BYTES, 16);
         const uint32_t b0 = desc_sw128_lo(sKV + kslot * C::TILE_BYTES, 16);
 #pragma unroll
         for (int kk = 0; kk < C::QK_STEPS; ++kk) {
-          const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
+          const uint32_t off = ((kk / C::K_PER_SPAN) * C::CHUNK_BYTES + (kk % C::K_PER_SPAN) * 32) >> 4;
           mma_ss_w(d_tmem, a0 + off, DESC_HI, b0 + off, DESC_HI, IDESC_QK, kk > 0 ? 1u : 0u, F8);
         }
       };
@@ -427,7 +432,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         const uint32_t b0 = desc_sw128_lo(sKV + vslot * C::TILE_BYTES, C::CHUNK_BYTES);
 #pragma unroll
         for (int kk = 0; kk < C::PV_STEPS; ++kk) {
-          mma_ts_w(d_tmem, a_tmem + kk * 8, b0 + ((kk * C::KSTEP * 128) >> 4), DESC_HI, IDESC_PV,
+          mma_ts_w(d_tmem, a_tmem + kk * 8, b0 + ((kk * C::KSTEP * C::SW) >> 4), DESC_HI, IDESC_PV,
                    (acc || kk > 0) ? 1u : 0u, F8);
         }
       };
@@ -804,7 +809,8 @@ attn_status launch_fwd(const void* q, const void* k, const void* v, FwdParams pr
                               static_cast<uint64_t>(bnhd ? len : H), static_cast<uint64_t>(B)};
     const uint64_t strides[3] = {D * elem, dims[1] * D * elem, dims[2] * dims[1] * D * elem};
     const uint32_t box[4] = {box_x, bnhd ? 1u : rows, bnhd ? rows : 1u, 1u};
-    return attn_internal::encode_tmap_4d(m, t, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    return attn_internal::encode_tmap_4d(m, t, base, dims, strides, box,
+                                         box_x * elem == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
   };
   if (!encode(&mq, dt, q, C::ELEM, C::CHUNK_ELEMS, kBM, N) || !encode(&mk, dt, k, C::ELEM, C::CHUNK_ELEMS, kBN, Nk) ||
       !encode(&mv, dt, v, C::ELEM, C::CHUNK_ELEMS, kBN, Nk) || !encode(&mo, dto, prm.o, 2, 64, kBM, N))

@@ -171,15 +171,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Untiled bulk copy global -> shared of `bytes` bytes (a multiple of 16; both
-// addresses 16-byte aligned), completing as transaction bytes on `bar`.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 // 4-D tiled store from shared memory (bulk-group completion); elements of the
 // box outside the tensor are not written.
 __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t src, int x, int y, int z,
@@ -278,6 +269,11 @@ __host__ __device__ constexpr uint32_t desc_sw128_hi(uint32_t sbo_bytes) {
 }
 __host__ __device__ constexpr uint32_t desc_sw128_lo(uint32_t saddr, uint32_t lbo_bytes) {
   return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes & 0x3FFFFu) >> 4) << 16);
+}
+// The same with 64-byte swizzle (layout type 4); the low word is laid out as
+// for 128-byte swizzle.
+__host__ __device__ constexpr uint32_t desc_sw64_hi(uint32_t sbo_bytes) {
+  return ((sbo_bytes & 0x3FFFFu) >> 4) | (1u << 14) | (4u << 29);
 }
 
 // The mbarrier at `bar` completes one arrival once every tcgen05 operation this

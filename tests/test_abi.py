@@ -152,7 +152,8 @@ def test_fp8_validation_before_launch(lib):
         return lib.attn_fwd_fp8(a["q8"], a["k8"], a["v8"], a["qs"], a["ks"], a["vs"], 0, a["o"],
                                 a["lse"], 1, 2, N, d, 0, scale, None)
 
-    assert prep(d=64) == attn.ATTN_ERR_UNSUPPORTED
+    for bad_d in (32, 96, 512):  # the pre-pass takes d = 64, 128, 256
+        assert prep(d=bad_d) == attn.ATTN_ERR_UNSUPPORTED
     assert prep(dtype=5) == attn.ATTN_ERR_UNSUPPORTED
     assert prep(q8=None) == attn.ATTN_ERR_INVALID_ARG
     assert prep(ks=None) == attn.ATTN_ERR_INVALID_ARG
@@ -160,7 +161,8 @@ def test_fp8_validation_before_launch(lib):
     assert prep(vs=0x9002) == attn.ATTN_ERR_MISALIGNED
     assert prep(signs=0xC008) == attn.ATTN_ERR_MISALIGNED
     assert prep(N=0) == attn.ATTN_OK
-    assert fwd(d=256) == attn.ATTN_ERR_UNSUPPORTED
+    for bad_d in (32, 96, 512):
+        assert fwd(d=bad_d) == attn.ATTN_ERR_UNSUPPORTED
     assert fwd(scale=float("nan")) == attn.ATTN_ERR_INVALID_ARG
     assert fwd(o=None) == attn.ATTN_ERR_INVALID_ARG
     assert fwd(v8=0x6001) == attn.ATTN_ERR_MISALIGNED
@@ -182,7 +184,7 @@ def test_fp8_rotary_validation_before_launch(lib):
     assert prep(cos=None, sin=None, N=0) == attn.ATTN_OK
     assert prep(cos=0xC004) == attn.ATTN_ERR_MISALIGNED
     assert prep(sin=0xD008) == attn.ATTN_ERR_MISALIGNED
-    assert prep(d=64) == attn.ATTN_ERR_UNSUPPORTED
+    assert prep(d=96) == attn.ATTN_ERR_UNSUPPORTED
     assert prep(N=0) == attn.ATTN_OK
 
 
