@@ -377,7 +377,6 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(dev)
     scale = d ** -0.5
     launches = [0]
-
     def step(causal=w["causal"]):
         attn.attn_fwd(qd, kd, vd, causal=causal, scale=scale, out=o, lse=lse, stream=stream)
         launches[0] += 1
@@ -425,15 +424,15 @@ def run_gpu(args):
     qp, kp, vp = q.pin_memory(), k.pin_memory(), v.pin_memory()
     op = torch.empty_like(qp).pin_memory()
     lp = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-    ws = torch.empty(attn.host_workspace_bytes(B, H, N, d, qd.dtype), dtype=torch.uint8, device=dev)
+    hws = torch.empty(attn.host_workspace_bytes(B, H, N, d, qd.dtype), dtype=torch.uint8, device=dev)
     e2e_steps = max(3, min(args.steps, 50))
     for _ in range(2):
-        attn.attn_fwd_host(qp, kp, vp, causal=w["causal"], scale=scale, workspace=ws, out=op,
+        attn.attn_fwd_host(qp, kp, vp, causal=w["causal"], scale=scale, workspace=hws, out=op,
                            lse=lp, device=dev)
     barrier(world)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        attn.attn_fwd_host(qp, kp, vp, causal=w["causal"], scale=scale, workspace=ws, out=op,
+        attn.attn_fwd_host(qp, kp, vp, causal=w["causal"], scale=scale, workspace=hws, out=op,
                            lse=lp, device=dev)
     e2e_s = max_over_ranks(time.perf_counter() - t0, world) / e2e_steps
     e2e_value = flops(w) * world / e2e_s / 1e12
@@ -457,6 +456,8 @@ def run_gpu(args):
             "config": {"workload": describe(w), "B": B, "H": H, "N": N, "d": d,
                        "causal": w["causal"], "scale": scale,
                        "flops_per_step_per_gpu": flops(w),
+                       "schedule": "persistent round-robin units" if not w["causal"]
+                                   else "persistent, longest-first causal units",
                        "l2": "inputs larger than L2 (Q, K, V, O = 4 x %.0f MiB)" % (B * H * N * d * 2 / 2 ** 20),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": roofline(achieved, traffic=traffic_from_profile(), kernel="attn_fwd_kernel<128, bf16>"),
@@ -537,7 +538,9 @@ def fp8_leg(w, dev, stream, rank, args, sampler=None):
     prep = lambda: attn.fp8_prepare(qd, kd, vd, signs=signs, out=bufs, stream=stream)
     rope = tuple(t.to(dev) for t in synth.rotary_tables(N, d))
     prep_rope = lambda: attn.fp8_prepare(qd, kd, vd, signs=signs, out=bufs, stream=stream, rope=rope)
-    fwd = lambda: attn.attn_fwd_fp8(*bufs, causal=w["causal"], scale=scale, out=o8, lse=l8, stream=stream)
+    ws = torch.empty(max(attn.workspace_bytes(d, dev), 1), dtype=torch.uint8, device=dev)
+    fwd = lambda: attn.attn_fwd_fp8(*bufs, causal=w["causal"], scale=scale, out=o8, lse=l8, stream=stream,
+                                    workspace=ws)
     def both():
         prep()
         fwd()
@@ -563,6 +566,9 @@ def fp8_leg(w, dev, stream, rank, args, sampler=None):
                        f"{'causal' if w['causal'] else 'non-causal'}, per-block scales + Hadamard, "
                        "inputs N(0,1) + N(0,100) * Bernoulli(0.001), bf16 output",
            "value": round(val, 2), "unit": UNIT, "launches": n,
+           "schedule": ("round-robin rounds plus a stream-K tail (attn_fwd_fp8_ws workspace; its arrival "
+                        "counters are zeroed by one cudaMemsetAsync before each launch)") if not w["causal"]
+                       else "persistent, longest-first causal units",
            "roofline": roofline(val, fp8=True, kernel="attn_fwd_kernel<128, e4m3>"),
            "clocks": clocks_fwd,
            "sustained": {"value": round(sus, 2), "launches": n_sus, "roofline": roofline(sus, fp8=True, sustained=True),

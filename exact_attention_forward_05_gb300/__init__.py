@@ -21,7 +21,7 @@ import torch
 
 from . import build as _build
 
-__all__ = ["attn_fwd", "attn_fwd_host", "fp8_prepare", "attn_fwd_fp8", "attn_fwd_fp8_pipeline", "host_workspace_bytes", "device_status",
+__all__ = ["attn_fwd", "workspace_bytes", "attn_fwd_host", "fp8_prepare", "attn_fwd_fp8", "attn_fwd_fp8_pipeline", "host_workspace_bytes", "device_status",
            "set_wait_timeout_ns", "set_schedule", "debug_bounded_wait", "debug_fail_host_chunk", "debug_exp2_poly",
            "attn_fwd_host_noalloc", "status_string", "library_path",
            "AttnError", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
@@ -74,6 +74,13 @@ def _load():
             lib.attn_fwd.restype = i32
             lib.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, i32, vp]
             lib.attn_fwd_ex.restype = i32
+            lib.attn_fwd_ws.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp]
+            lib.attn_fwd_ws.restype = i32
+            lib.attn_fwd_workspace_bytes.argtypes = [i32]
+            lib.attn_fwd_workspace_bytes.restype = sz
+            lib.attn_fwd_fp8_ws.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
+                                            i32, f32, vp, sz, vp]
+            lib.attn_fwd_fp8_ws.restype = i32
             lib.attn_fwd_host_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
             lib.attn_fwd_host_workspace_bytes.restype = sz
             lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32,
@@ -169,10 +176,23 @@ def _qkv_shapes(q, k, v, layout):
     return int(B), int(H), int(Nq), int(Nk), int(d)
 
 
+def workspace_bytes(d: int, device=None) -> int:
+    """Bytes of the workspace that balances full attention over the SMs
+    (attn_fwd_workspace_bytes) for head dimension d on ``device``."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(device):
+        return int(_load().attn_fwd_workspace_bytes(int(d)))
+
+
+def _check_workspace(ws, device):
+    if ws.dtype != torch.uint8 or not ws.is_contiguous() or ws.device != device:
+        raise ValueError("workspace must be a contiguous uint8 tensor on q's device")
+
+
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal=False,
              scale: float | None = None, out: torch.Tensor | None = None,
              lse: torch.Tensor | None = None, return_lse: bool = True, stream=None,
-             layout: str = "bhnd"):
+             layout: str = "bhnd", workspace: torch.Tensor | None = None):
     """Exact attention forward on CUDA tensors (fp16 or bf16).
 
     q: [B, H, Nq, d], k, v: [B, H, Nk, d]; with ``layout="bnhd"`` they are
@@ -180,7 +200,9 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal=False,
     True (query i sees keys j <= i) or "bottom_right" (query i sees keys
     j <= i + Nk - Nq: the queries are the last Nq positions).  Returns (O, lse)
     with O like q and lse float32 [B, H, Nq] in either layout (None when
-    ``return_lse`` is false and no ``lse`` buffer is given).
+    ``return_lse`` is false and no ``lse`` buffer is given).  ``workspace``
+    (uint8 CUDA tensor of workspace_bytes(d)) selects attn_fwd_ws, which
+    balances full self-attention in [B, H, N, d] over the SMs.
     """
     if layout not in _LAYOUTS:
         raise ValueError("layout must be 'bhnd' or 'bnhd'")
@@ -200,6 +222,17 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal=False,
     if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous()
                             or tuple(lse.shape) != (B, H, N) or lse.device != q.device):
         raise ValueError("lse must be a contiguous float32 [B, H, N] tensor on q's device")
+    if workspace is not None:
+        if layout != "bhnd" or N != Nk or mode == CAUSAL_BOTTOM_RIGHT:
+            raise ValueError("a workspace is taken for [B, H, N, d] self-attention only")
+        _check_workspace(workspace, q.device)
+        with torch.cuda.device(q.device):
+            st = _load().attn_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                     None if lse is None else lse.data_ptr(), B, H, N, d, mode,
+                                     float(scale), _DTYPES[q.dtype], workspace.data_ptr(),
+                                     workspace.numel(), _stream_handle(stream, q.device))
+        _check(st, "attn_fwd_ws")
+        return out, lse
     with torch.cuda.device(q.device):
         st = _load().attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                  None if lse is None else lse.data_ptr(), B, H, N, Nk, d,
@@ -294,9 +327,11 @@ def fp8_prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, signs: torch.
 
 def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False,
                  scale: float | None = None, out: torch.Tensor | None = None,
-                 lse: torch.Tensor | None = None, return_lse: bool = True, stream=None):
-    """Exact attention on E4M3 codes (uint8 [B, H, N, 128]) and float32 scales
-    (per block [B, H, ceil(N/128)] or per tensor [1]); bf16 output."""
+                 lse: torch.Tensor | None = None, return_lse: bool = True, stream=None,
+                 workspace: torch.Tensor | None = None):
+    """Exact attention on E4M3 codes (uint8 [B, H, N, d], d = 64, 128, 256)
+    and float32 scales (per block [B, H, ceil(N/128)] or per tensor [1]); bf16
+    output.  ``workspace`` as for attn_fwd (attn_fwd_fp8_ws)."""
     if q8.dim() != 4 or q8.shape != k8.shape or q8.shape != v8.shape:
         raise ValueError("q8, k8, v8 must share one [B, H, N, d] shape")
     B, H, N, d = (int(s_) for s_ in q8.shape)
@@ -307,12 +342,16 @@ def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False,
         out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
     if lse is None and return_lse:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    if workspace is not None:
+        _check_workspace(workspace, q8.device)
     with torch.cuda.device(q8.device):
-        st = _load().attn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), q_scale.data_ptr(),
-                                  k_scale.data_ptr(), v_scale.data_ptr(), int(per_tensor),
-                                  out.data_ptr(), None if lse is None else lse.data_ptr(),
-                                  B, H, N, d, int(bool(causal)), float(scale),
-                                  _stream_handle(stream, q8.device))
+        st = _load().attn_fwd_fp8_ws(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), q_scale.data_ptr(),
+                                     k_scale.data_ptr(), v_scale.data_ptr(), int(per_tensor),
+                                     out.data_ptr(), None if lse is None else lse.data_ptr(),
+                                     B, H, N, d, int(bool(causal)), float(scale),
+                                     None if workspace is None else workspace.data_ptr(),
+                                     0 if workspace is None else workspace.numel(),
+                                     _stream_handle(stream, q8.device))
     _check(st, "attn_fwd_fp8")
     return out, lse
 
@@ -336,7 +375,7 @@ def set_wait_timeout_ns(ns: int) -> None:
     _load().attn_set_wait_timeout_ns(int(ns))
 
 
-SCHEDULE_PINGPONG, SCHEDULE_ONE_TILE = 0, 1
+SCHEDULE_PINGPONG, SCHEDULE_ONE_TILE, SCHEDULE_BALANCED = 0, 1, 2
 
 
 def set_schedule(mode: int) -> None:

@@ -374,10 +374,10 @@ ATTN_EXPORT attn_status attn_fp8_prepare(const void* q, const void* k, const voi
                                  per_tensor, nullptr, nullptr, 0, B, H, N, d, stream);
 }
 
-ATTN_EXPORT attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale,
-                                     const float* k_scale, const float* v_scale, int per_tensor, void* o,
-                                     float* lse, int B, int H, int N, int d, int causal, float scale,
-                                     void* stream) {
+ATTN_EXPORT attn_status attn_fwd_fp8_ws(const void* q8, const void* k8, const void* v8, const float* q_scale,
+                                        const float* k_scale, const float* v_scale, int per_tensor, void* o,
+                                        float* lse, int B, int H, int N, int d, int causal, float scale,
+                                        void* workspace, size_t workspace_bytes, void* stream) {
   attn_status st = check_common(B, H, N);
   if (st != ATTN_OK) return st;
   if (!fwd_fp8_head_dim(d)) return ATTN_ERR_UNSUPPORTED;
@@ -398,10 +398,21 @@ ATTN_EXPORT attn_status attn_fwd_fp8(const void* q8, const void* k8, const void*
   const int nblk = (N + kQuantRows - 1) / kQuantRows;
   prm.scale_bh_stride = per_tensor ? 0 : nblk;
   prm.scale_blk_stride = per_tensor ? 0 : 1;
+  if (workspace != nullptr && !attn_internal::aligned(workspace, 256)) return ATTN_ERR_MISALIGNED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* w = workspace;
+  const size_t wb = workspace_bytes;
   switch (d) {
-    case 64: return attn_kernel::launch_fwd<64, KIND_E4M3>(q8, k8, v8, prm, B, H, N, N, scale, s);
-    case 128: return attn_kernel::launch_fwd<128, KIND_E4M3>(q8, k8, v8, prm, B, H, N, N, scale, s);
-    default: return attn_kernel::launch_fwd<256, KIND_E4M3>(q8, k8, v8, prm, B, H, N, N, scale, s);
+    case 64: return attn_kernel::launch_fwd<64, KIND_E4M3>(q8, k8, v8, prm, B, H, N, N, scale, s, w, wb);
+    case 128: return attn_kernel::launch_fwd<128, KIND_E4M3>(q8, k8, v8, prm, B, H, N, N, scale, s, w, wb);
+    default: return attn_kernel::launch_fwd<256, KIND_E4M3>(q8, k8, v8, prm, B, H, N, N, scale, s, w, wb);
   }
+}
+
+ATTN_EXPORT attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale,
+                                     const float* k_scale, const float* v_scale, int per_tensor, void* o,
+                                     float* lse, int B, int H, int N, int d, int causal, float scale,
+                                     void* stream) {
+  return attn_fwd_fp8_ws(q8, k8, v8, q_scale, k_scale, v_scale, per_tensor, o, lse, B, H, N, d, causal, scale,
+                         nullptr, 0, stream);
 }

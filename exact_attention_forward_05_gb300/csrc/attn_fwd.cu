@@ -16,14 +16,15 @@ namespace {
 
 template <int D, int KIND>
 attn_status launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                   int Nq, int Nk, int causal, float scale, int layout, cudaStream_t stream) {
+                   int Nq, int Nk, int causal, float scale, int layout, cudaStream_t stream,
+                   void* ws = nullptr, size_t ws_bytes = 0) {
   FwdParams prm{};
   prm.o = o;
   prm.lse = lse;
   prm.causal = causal != ATTN_CAUSAL_NONE;
   prm.causal_off = causal == ATTN_CAUSAL_BOTTOM_RIGHT ? Nk - Nq : 0;
   prm.layout = layout;
-  return attn_kernel::launch_fwd<D, KIND>(q, k, v, prm, B, H, Nq, Nk, scale, stream);
+  return attn_kernel::launch_fwd<D, KIND>(q, k, v, prm, B, H, Nq, Nk, scale, stream, ws, ws_bytes);
 }
 
 __global__ void debug_wait_kernel(uint64_t timeout_ns) {
@@ -73,7 +74,7 @@ attn_status check_args(const void* q, const void* k, const void* v, const void* 
   return ATTN_OK;
 }
 
-size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+using attn_kernel::align256;
 
 // Longest query or key sequence attn_fwd_ex takes: row and key indices plus a
 // tile stay inside int arithmetic in the kernel.
@@ -106,6 +107,33 @@ ATTN_EXPORT attn_status attn_fwd_ex(const void* q, const void* k, const void* v,
                         : launch<128, KIND_F16>(q, k, v, o, lse, B, H, Nq, Nk, causal, scale, layout, s);
     default: return bf ? launch<256, KIND_BF16>(q, k, v, o, lse, B, H, Nq, Nk, causal, scale, layout, s)
                        : launch<256, KIND_F16>(q, k, v, o, lse, B, H, Nq, Nk, causal, scale, layout, s);
+  }
+}
+
+ATTN_EXPORT size_t attn_fwd_workspace_bytes(int d) {
+  if (d != 64 && d != 128 && d != 256) return 0;
+  return attn_kernel::stream_k_ws_bytes(d, attn_internal::sm_count());
+}
+
+ATTN_EXPORT attn_status attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                    int H, int N, int d, int causal, float scale, attn_dtype dtype,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  attn_status st = check_args(q, k, v, o, lse, B, H, N, d, scale, dtype);
+  if (st != ATTN_OK || static_cast<int64_t>(B) * H * N == 0) return st;
+  if (N > kMaxRows) return ATTN_ERR_UNSUPPORTED;
+  if (workspace != nullptr && !attn_internal::aligned(workspace, 256)) return ATTN_ERR_MISALIGNED;
+  const int cm = causal ? ATTN_CAUSAL_TOP_LEFT : ATTN_CAUSAL_NONE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool bf = dtype == ATTN_BF16;
+  void* w = workspace;
+  const size_t wb = workspace_bytes;
+  switch (d) {
+    case 64: return bf ? launch<64, KIND_BF16>(q, k, v, o, lse, B, H, N, N, cm, scale, ATTN_LAYOUT_BHND, s, w, wb)
+                       : launch<64, KIND_F16>(q, k, v, o, lse, B, H, N, N, cm, scale, ATTN_LAYOUT_BHND, s, w, wb);
+    case 128: return bf ? launch<128, KIND_BF16>(q, k, v, o, lse, B, H, N, N, cm, scale, ATTN_LAYOUT_BHND, s, w, wb)
+                        : launch<128, KIND_F16>(q, k, v, o, lse, B, H, N, N, cm, scale, ATTN_LAYOUT_BHND, s, w, wb);
+    default: return bf ? launch<256, KIND_BF16>(q, k, v, o, lse, B, H, N, N, cm, scale, ATTN_LAYOUT_BHND, s, w, wb)
+                       : launch<256, KIND_F16>(q, k, v, o, lse, B, H, N, N, cm, scale, ATTN_LAYOUT_BHND, s, w, wb);
   }
 }
 

@@ -78,6 +78,10 @@ constexpr int kBM = 128;  // query rows per Q tile (= TMEM lanes)
 constexpr int kBN = 128;  // keys per K/V block
 constexpr float kRescaleThreshold = 8.0f;
 
+// Most CTAs whose stream-K ranges share one unit: the host cuts at least
+// half a unit's key blocks per CTA, so a unit meets at most three ranges.
+constexpr int kMaxParts = 3;
+
 #ifndef ATTN_FP8_POLY_QUADS
 #define ATTN_FP8_POLY_QUADS 0
 #endif
@@ -141,7 +145,10 @@ struct Cfg {
   static constexpr int OST_BYTES = kBM * 128;
   static constexpr int OFF_OST = OFF_KV + STAGES * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_OST + NQ * OST_BYTES;
-  static constexpr int SMEM_BYTES = OFF_BAR + 8 * NBARS + 16 + 1024;
+  // After the barriers: TMEM address, abort flag, two last-part flags, then
+  // the stream-K segment list.
+  static constexpr int OFF_SEGS = OFF_BAR + 8 * NBARS + 16;
+  static constexpr int SMEM_BYTES = OFF_SEGS + 64 + 1024;
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(SMEM_BYTES > 114 * 1024, "one CTA per SM (TMEM is allocated whole)");
   static_assert(ROW_BYTES % SW == 0, "rows span whole swizzle spans");
@@ -166,11 +173,28 @@ struct FwdParams {
   const float* k_scale;
   const float* v_scale;
   int scale_bh_stride, scale_blk_stride;
+  // Stream-K tail (full attention, two Q tiles, with a workspace): units
+  // [0, sk_unit0) run round-robin in whole rounds; the (unit, key block)
+  // steps of the rest are cut into gridDim.x equal contiguous ranges, one per
+  // CTA, so every CTA ends after the same number of key blocks.  A unit cut between CTAs is done in parts: every part writes its
+  // unnormalised O, running maximum m and sum l to its slot in the workspace,
+  // and the last part to finish (an arrival counter per unit tile) combines
+  // them and writes O and lse.  CTA c owns slots 2c (the unit its range
+  // starts in) and 2c + 1 (the unit it ends in), and the counter pair of the
+  // unit its range starts in.
+  int stream_k;         // 0 = round-robin units
+  int sk_unit0;         // stream-K: first unit of the tail cut into ranges
+  float* ws_o;          // [slot][tile][d/4][128 rows][4] float
+  float* ws_ml;         // [slot][tile][m | l][128 rows] float
+  unsigned int* ws_cnt; // [cta][tile] arrivals, zero at launch
 };
 
 struct Unit {
   int bh, m0, nkb;
-  int nb[2];  // key blocks visited by each Q tile (0 = tile inactive)
+  int nb[2];  // key blocks visited by each Q tile: [jb, nb[t]) (nb[t] = 0: tile inactive)
+  int jb;     // first key block (0 unless a stream-K part)
+  int u;      // unit index
+  bool part;  // stream-K: only some of the unit's key blocks
 };
 
 // Tensor maps are 4-D over the operand as it lies in memory: [B, H, N, d] as
@@ -195,10 +219,13 @@ template <int NQ>
 __device__ __forceinline__ Unit decode_unit(int e, const FwdParams& p) {
   Unit w;
   int u = e, half = -1;
+  w.jb = 0;
+  w.part = false;
   if (e >= p.full_units) {
     u = p.full_units + (e - p.full_units) / 2;
     half = (e - p.full_units) & 1;
   }
+  w.u = u;
   int qu;
   if (p.causal) {
     qu = p.units_per_head - 1 - u / p.BH;
@@ -227,6 +254,85 @@ __device__ __forceinline__ int unit_of_round(int r, int num_units) {
   const int u = r * G + ((r & 1) ? (G - 1 - c) : c);
   return u < num_units ? u : -1;
 }
+
+// Stream-K part of the schedule: the (unit x key block) steps of units
+// [sk_unit0, num_units), cut into gridDim.x equal contiguous ranges.
+struct SkSpan {
+  int64_t base, total;  // first step, number of steps
+  __device__ __forceinline__ SkSpan(const FwdParams& p, int nkb)
+      : base(static_cast<int64_t>(p.sk_unit0) * nkb), total(static_cast<int64_t>(p.num_units - p.sk_unit0) * nkb) {}
+  // First step of CTA c's range.
+  __device__ __forceinline__ int64_t begin(int c) const {
+    return base + total * c / static_cast<int64_t>(gridDim.x);
+  }
+  // The CTA whose range holds step `pos`.
+  __device__ __forceinline__ int cta_of(int64_t pos) const {
+    const int G = static_cast<int>(gridDim.x);
+    int c = static_cast<int>((pos - base) * G / total);
+    while (c + 1 < G && begin(c + 1) <= pos) ++c;
+    while (c > 0 && begin(c) > pos) --c;
+    return c;
+  }
+  // Workspace slot of CTA c's part of unit u: 2c for the unit its range
+  // starts in, 2c + 1 for the unit it ends in.
+  __device__ __forceinline__ int slot(int c, int u, int nkb) const {
+    return 2 * c + (static_cast<int64_t>(u) != begin(c) / nkb ? 1 : 0);
+  }
+};
+
+// Stream-K segments of one CTA (at most kMaxSegs: its range holds less than
+// 1.5 units' key blocks): unit, first and end key block.  Computed once per
+// CTA by one thread into shared memory, so that the roles iterating over them
+// keep only an index in registers.
+constexpr int kMaxSegs = 3;
+struct SkSegs {
+  int n;
+  int u[kMaxSegs], jb[kMaxSegs], je[kMaxSegs];
+};
+__device__ __forceinline__ void sk_segments(const FwdParams& p, SkSegs* out) {
+  const int nkb = (p.Nk + kBN - 1) / kBN;
+  const SkSpan sk(p, nkb);
+  int64_t pos = sk.begin(blockIdx.x);
+  const int64_t end = sk.begin(blockIdx.x + 1);
+  int n = 0;
+  while (pos < end && n < kMaxSegs) {
+    const int u = static_cast<int>(pos / nkb);
+    const int jb = static_cast<int>(pos - static_cast<int64_t>(u) * nkb);
+    const int je = static_cast<int>(min(static_cast<int64_t>(nkb), jb + (end - pos)));
+    out->u[n] = u;
+    out->jb[n] = jb;
+    out->je[n] = je;
+    ++n;
+    pos += je - jb;
+  }
+  out->n = n;
+}
+
+// The work of one CTA, the same sequence for every role: whole units in
+// persistent round-robin (snake) order -- units [0, sk_unit0) when the
+// stream-K tail is on -- then, with it, the CTA's stream-K segments.
+struct WorkIter {
+  int r = 0, seg = 0;
+  template <int NQ>
+  __device__ __forceinline__ bool next(Unit& w, const FwdParams& p, const SkSegs* segs) {
+    const int rr_units = p.stream_k ? p.sk_unit0 : p.num_units;
+    while (r * static_cast<int>(gridDim.x) < rr_units) {
+      const int u = unit_of_round(r++, rr_units);
+      if (u < 0) continue;
+      w = decode_unit<NQ>(u, p);
+      return true;
+    }
+    if (!p.stream_k || seg >= segs->n) return false;
+    const int je = segs->je[seg];
+    w = decode_unit<NQ>(segs->u[seg], p);
+    if (w.nb[0] > 0) w.nb[0] = je;
+    if (w.nb[1] > 0) w.nb[1] = je;
+    w.jb = segs->jb[seg];
+    w.part = w.jb > 0 || je < w.nkb;
+    ++seg;
+    return true;
+  }
+};
 
 // Two weights -> one 32-bit TMEM column of 16-bit P (first key in the low half).
 template <int KIND>
@@ -275,8 +381,12 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
 
   const int warp = static_cast<int>(warp_id());
   const int lane = static_cast<int>(lane_id());
+  SkSegs* segs = reinterpret_cast<SkSegs*>(smem + C::OFF_SEGS);
+  static_assert(sizeof(SkSegs) <= 64, "segment list space");
 
   if (threadIdx.x == 0) {
+    if (p.stream_k) sk_segments(p, segs);
+    else segs->n = 0;
     mbar_init(BAR(C::B_Q_FULL), 1);
     mbar_init(BAR(C::B_Q_EMPTY), 1);
     for (int s = 0; s < C::STAGES; ++s) {
@@ -331,13 +441,13 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         return true;
       };
       // Pair slot s holds K_j in tile 2s and V_{j-1} in tile 2s+1 (either may
-      // be absent at the ends of a unit: step 0 has no V, step nbmax no K).
-      auto load_pair = [&](int j, int nbmax, int ub, int uh) -> bool {
+      // be absent at the ends of a unit: step jb has no V, step nbmax no K).
+      auto load_pair = [&](int j, int jb, int nbmax, int ub, int uh) -> bool {
         const uint32_t s = kv_fill % C::RING;
         const uint32_t ph = (kv_fill / C::RING) & 1u;
         if (!mbar_wait(BAR(C::B_KV_EMPTY + s), ph ^ 1u, wc, attn_internal::kStatusTimeoutLoad))
           return false;
-        const bool has_k = j < nbmax, has_v = j >= 1;
+        const bool has_k = j < nbmax, has_v = j > jb;
         mbar_arrive_expect_tx(BAR(C::B_KV_FULL + s), (has_k + has_v) * C::TILE_BYTES);
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c) {
@@ -351,11 +461,8 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         ++kv_fill;
         return true;
       };
-      for (int r = 0; ok; ++r) {
-        if (r * static_cast<int>(gridDim.x) >= p.num_units) break;
-        const int u = unit_of_round(r, p.num_units);
-        if (u < 0) continue;
-        const Unit w = decode_unit<NQ>(u, p);
+      WorkIter wi;
+      for (Unit w; ok && wi.next<NQ>(w, p, segs);) {
         const int nbmax = max(w.nb[0], w.nb[1]);
         if (nbmax == 0) continue;  // no query row of this entry is below N
         const int ub = w.bh / p.H, uh = w.bh - ub * p.H;
@@ -374,9 +481,10 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
                           c * C::CHUNK_ELEMS, w.m0 + kBM * t, ub, uh, bnhd);
         }
         // K/V in the order the MMA warp consumes them: K_0, then (K_j, V_{j-1}).
-        for (int j = 0; j <= nbmax && ok; ++j) {
+        const int jb = w.jb;
+        for (int j = jb; j <= nbmax && ok; ++j) {
           if constexpr (C::KV_PAIRS) {
-            ok = load_pair(j, nbmax, ub, uh);
+            ok = load_pair(j, jb, nbmax, ub, uh);
           } else {
             if (j < nbmax) ok = load_block(&tmK, j, ub, uh);
             if (ok && j >= 1) ok = load_block(&tmV, j - 1, ub, uh);
@@ -443,11 +551,8 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         return true;
       };
 
-      for (int r = 0; ok; ++r) {
-        if (r * static_cast<int>(gridDim.x) >= p.num_units) break;
-        const int u = unit_of_round(r, p.num_units);
-        if (u < 0) continue;
-        const Unit w = decode_unit<NQ>(u, p);
+      WorkIter wi;
+      for (Unit w; ok && wi.next<NQ>(w, p, segs);) {
         const int nbmax = max(w.nb[0], w.nb[1]);
         if (nbmax == 0) continue;
         if (!mbar_wait(BAR(C::B_Q_FULL), q_iter & 1u, wc, attn_internal::kStatusTimeoutMma)) { ok = false; break; }
@@ -473,16 +578,20 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
               mma_commit(BAR(C::B_S_FULL + t));
             }
           mma_commit(BAR(C::B_KV_EMPTY + ps));
-          if (nbmax == 1) mma_commit(BAR(C::B_Q_EMPTY));
-          for (int j = 1; j <= nbmax && ok; ++j) {
+          const int jb = w.jb, nb0 = w.nb[0], nb1 = w.nb[1];
+          if (nbmax - jb == 1) mma_commit(BAR(C::B_Q_EMPTY));
+          for (int j = jb + 1; j <= nbmax && ok; ++j) {
             if (!(ok = next_pair(ps))) break;
-            for (int t = 0; t < 2 && ok; ++t) {
-              if (j - 1 < w.nb[t]) {
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const int nbt = t ? nb1 : nb0;
+              if (!ok) break;
+              if (j - 1 < nbt) {
                 if (!(ok = wait_p(t))) break;
-                issue_pv(t, t, 2 * ps + 1, j - 1 > 0);
-                if (!C::LAST_O_DONE_ONLY || j >= w.nb[t]) mma_commit(BAR(C::B_O_DONE + t));
+                issue_pv(t, t, 2 * ps + 1, j - 1 > jb);
+                if (!C::LAST_O_DONE_ONLY || j >= nbt) mma_commit(BAR(C::B_O_DONE + t));
               }
-              if (j < w.nb[t]) {
+              if (j < nbt) {
                 issue_qk(t, t, 2 * ps);
                 mma_commit(BAR(C::B_S_FULL + t));
               }
@@ -531,12 +640,10 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
     uint32_t sph = 0u, oph = 0u;  // sph bit b: wait parity of S_FULL[b]
     bool ok = true;
 
-    for (int r = 0; ok; ++r) {
-      if (r * static_cast<int>(gridDim.x) >= p.num_units) break;
-      const int u = unit_of_round(r, p.num_units);
-      if (u < 0) continue;
-      const Unit w = decode_unit<NQ>(u, p);
-      const int nb = w.nb[wg];
+    WorkIter wi;
+    for (Unit w; ok && wi.next<NQ>(w, p, segs);) {
+      const int nb = wg ? w.nb[1] : w.nb[0];
+      const int jb = w.jb;
       if (nb == 0) continue;
       const int tile_row0 = w.m0 + wg * kBM;
       const int qi = tile_row0 + row;                  // query row of this thread
@@ -550,13 +657,13 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         c_q = p.sl2 * p.q_scale[sb + (tile_row0 / kBM) * p.scale_blk_stride];
         // The lanes share the nb scale loads, then reduce across the warp.
         float mx = 0.f;
-        for (int j = lane; j < nb; j += 32) mx = fmaxf(mx, p.v_scale[sb + j * p.scale_blk_stride]);
+        for (int j = jb + lane; j < nb; j += 32) mx = fmaxf(mx, p.v_scale[sb + j * p.scale_blk_stride]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         sv_max = mx > 0.f ? mx : 1.f;
       }
 
-      for (int j = 0; j < nb; ++j) {
+      for (int j = jb; j < nb; ++j) {
         const int b = NQ == 2 ? wg : (j & 1);
         // Per-block multiplier of S and the V fold (FP8); plain scale otherwise.
         float cj = c_q, lg2_ratio = 0.f, inv_ratio = 1.f;
@@ -625,7 +732,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
 
         float alpha = 1.f;
         bool rescale = false;
-        if (j == 0) {
+        if (j == jb) {
           m_used = (mblk == -INFINITY) ? 0.f : mblk;
         } else if (mblk > m_used + kRescaleThreshold) {
           alpha = ex2(m_used - mblk);
@@ -694,7 +801,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
           rowsum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
         }
 
-        if (j > 0) {
+        if (j > jb) {
           // O holds P_{j-1} V_{j-1} once the previous product has completed.
           if constexpr (!C::LAST_O_DONE_ONLY) {
             if (!(ok = mbar_wait_warp(BAR(C::B_O_DONE + wg), oph, wc, attn_internal::kStatusTimeoutSoftmax))) break;
@@ -735,7 +842,77 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
       }
       oph ^= 1u;
       tc_fence_after();
-      const float inv_l = sv_max / l;
+      float inv_l = sv_max / l;
+      float lse_m = m_used, lse_l = l;
+      // Stream-K part: publish this part, and combine if it is the last one.
+      int parts = 0;
+      const float* part_o[kMaxParts] = {};
+      float part_w[kMaxParts] = {};
+      if constexpr (NQ == 2) {
+        if (w.part) {
+          const SkSpan sk(p, w.nkb);
+          const int c_first = sk.cta_of(static_cast<int64_t>(w.u) * w.nkb);
+          const int c_last = sk.cta_of(static_cast<int64_t>(w.u) * w.nkb + w.nkb - 1);
+          const int me = static_cast<int>(blockIdx.x);
+          const size_t tile_o = static_cast<size_t>(D) * kBM, tile_ml = 2 * kBM;
+          const int my_slot = sk.slot(me, w.u, w.nkb);
+          float* po = p.ws_o + (static_cast<size_t>(my_slot) * 2 + wg) * tile_o;
+          float* pml = p.ws_ml + (static_cast<size_t>(my_slot) * 2 + wg) * tile_ml;
+          // This part's O (at its true scale, times svmax for FP8), m and l.
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tm_o + 32 * c, o);
+            tmem_wait_ld(o);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+              *reinterpret_cast<float4*>(po + ((8 * c + q4) * kBM + row) * 4) =
+                  make_float4(__uint_as_float(o[4 * q4]) * sv_max, __uint_as_float(o[4 * q4 + 1]) * sv_max,
+                              __uint_as_float(o[4 * q4 + 2]) * sv_max, __uint_as_float(o[4 * q4 + 3]) * sv_max);
+          }
+          pml[row] = m_used;
+          pml[kBM + row] = l;
+          __threadfence();
+          bar_sync_n(tile_bar, 128);
+          volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2 + wg);
+          if (wq == 0 && lane == 0) {
+            const unsigned int old = atomicAdd(p.ws_cnt + 2 * c_last + wg, 1u);
+            *last_flag = old + 1 == static_cast<unsigned int>(c_last - c_first + 1) ? 1 : 0;
+          }
+          bar_sync_n(tile_bar, 128);
+          if (!*last_flag) {
+            tc_fence_before();
+            continue;  // another part of this unit tile finishes later and combines
+          }
+          __threadfence();
+          // Every part of this unit tile is in the workspace (this one too).
+          parts = c_last - c_first + 1;
+          float M = -INFINITY, mp[kMaxParts], lp[kMaxParts];
+#pragma unroll
+          for (int q = 0; q < kMaxParts; ++q) {
+            mp[q] = -INFINITY;
+            lp[q] = 0.f;
+            if (q < parts) {
+              const int slot = sk.slot(c_first + q, w.u, w.nkb);
+              const float* ml = p.ws_ml + (static_cast<size_t>(slot) * 2 + wg) * tile_ml;
+              mp[q] = __ldcg(ml + row);
+              lp[q] = __ldcg(ml + kBM + row);
+              part_o[q] = p.ws_o + (static_cast<size_t>(slot) * 2 + wg) * tile_o;
+              M = fmaxf(M, mp[q]);
+            }
+          }
+          float L = 0.f;
+#pragma unroll
+          for (int q = 0; q < kMaxParts; ++q)
+            if (q < parts) {
+              part_w[q] = ex2(mp[q] - M);
+              L += part_w[q] * lp[q];
+            }
+          inv_l = 1.f / L;
+          lse_m = M;
+          lse_l = L;
+        }
+      }
       const uint32_t ost = smem_u32(smem + C::OFF_OST + wg * C::OST_BYTES);
       const uint32_t ost_row = ost + static_cast<uint32_t>(row) * 128u;
       const uint32_t swz = static_cast<uint32_t>(row & 7);
@@ -743,10 +920,32 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
 #pragma unroll 1
       for (int c2 = 0; c2 < D / 64; ++c2) {
         uint32_t o[2][32];
-        tmem_ld32(tm_o + 64 * c2, o[0]);
-        tmem_ld32(tm_o + 64 * c2 + 32, o[1]);
-        tmem_wait_ld(o[0]);
-        reg_pin(o[1]);
+        if (parts > 0) {
+          // Combined O: the parts' weighted sum (their slots are in L2).
+#pragma unroll
+          for (int q4 = 0; q4 < 16; ++q4) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < kMaxParts; ++q)
+              if (q < parts) {
+                const float4 v4 = __ldcg(reinterpret_cast<const float4*>(part_o[q] + ((16 * c2 + q4) * kBM + row) * 4));
+                acc.x = fmaf(part_w[q], v4.x, acc.x);
+                acc.y = fmaf(part_w[q], v4.y, acc.y);
+                acc.z = fmaf(part_w[q], v4.z, acc.z);
+                acc.w = fmaf(part_w[q], v4.w, acc.w);
+              }
+            const int h = q4 >> 3, i = (q4 & 7) * 4;
+            o[h][i] = __float_as_uint(acc.x);
+            o[h][i + 1] = __float_as_uint(acc.y);
+            o[h][i + 2] = __float_as_uint(acc.z);
+            o[h][i + 3] = __float_as_uint(acc.w);
+          }
+        } else {
+          tmem_ld32(tm_o + 64 * c2, o[0]);
+          tmem_ld32(tm_o + 64 * c2 + 32, o[1]);
+          tmem_wait_ld(o[0]);
+          reg_pin(o[1]);
+        }
         // The previous bulk store from this buffer must have read it.
         if (wq == 0 && lane == 0) bulk_wait_read_all();
         bar_sync_n(tile_bar, 128);
@@ -771,7 +970,7 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         }
       }
       if (qi < p.N && p.lse != nullptr)
-        p.lse[static_cast<size_t>(w.bh) * p.N + qi] = (m_used + log2f(l)) * 0.69314718055994531f;
+        p.lse[static_cast<size_t>(w.bh) * p.N + qi] = (lse_m + log2f(lse_l)) * 0.69314718055994531f;
       tc_fence_before();
     }
   }
@@ -787,11 +986,28 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
   }
 }
 
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Workspace of the stream-K schedule on a GPU with `sms` multiprocessors:
+// two slots per CTA of (two tiles x (128 x D floats of O, 128 m, 128 l)),
+// then two arrival counters per CTA.  0 where the schedule is not used (one
+// Q tile per CTA, d = 256).
+inline size_t stream_k_ws_bytes(int D, int sms) {
+  if (D > 128 || sms <= 0) return 0;
+  const size_t slots = 2 * static_cast<size_t>(sms);
+  return align256(slots * 2 * D * kBM * 4) + align256(slots * 2 * 2 * kBM * 4) +
+         align256(static_cast<size_t>(sms) * 2 * 4);
+}
+
 // Host side: encode the three tensor maps, set the shared-memory attribute
-// once per device, and launch one CTA per SM (or per unit, if fewer).
+// once per device, and launch one CTA per SM (or per unit, if fewer).  With
+// a workspace of at least stream_k_ws_bytes(D, SMs) bytes (256-byte aligned),
+// full attention over at least one unit per SM whose units do not divide
+// evenly over the SMs runs the stream-K schedule.
 template <int D, int KIND>
 attn_status launch_fwd(const void* q, const void* k, const void* v, FwdParams prm, int B, int H,
-                       int N, int Nk, float scale, cudaStream_t stream) {
+                       int N, int Nk, float scale, cudaStream_t stream, void* ws = nullptr,
+                       size_t ws_bytes = 0) {
   using C = Cfg<D, KIND>;
   const CUtensorMapDataType dt = KIND == KIND_E4M3   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                  : KIND == KIND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -841,7 +1057,33 @@ attn_status launch_fwd(const void* q, const void* k, const void* v, FwdParams pr
   // half units (one Q tile each, one per CTA), so that round costs half a unit.
   prm.full_units = units;
   prm.num_units = units;
-  if (C::NQ == 2 && attn_internal::schedule_mode() == ATTN_SCHEDULE_ONE_TILE) {
+  prm.stream_k = 0;
+  const size_t sk_bytes = stream_k_ws_bytes(D, sms);
+  // Stream-K tail by default only for the FP8 kernel: on the bench shapes it
+  // measured faster there and slower for the 16-bit kernels (whose longer
+  // key-block steps leave the tail less to gain than the parts cost);
+  // ATTN_SCHEDULE_BALANCED takes it for every kind.
+  const int mode = attn_internal::schedule_mode();
+  const bool sk_kind = KIND == KIND_E4M3 || mode == ATTN_SCHEDULE_BALANCED;
+  if (C::NQ == 2 && !prm.causal && ws != nullptr && sk_bytes > 0 && ws_bytes >= sk_bytes && sk_kind &&
+      mode != ATTN_SCHEDULE_ONE_TILE && units >= sms && units % sms != 0) {
+    // The last `tail` units go to stream-K (at least half a round, so every
+    // range holds half a unit's key blocks or more); the rest run in whole
+    // round-robin rounds, head-major, so that CTAs working at the same time
+    // share K and V through L2.
+    const int rest = units % sms;
+    const int tail = 2 * rest >= sms ? rest : rest + sms;
+    const size_t slots = 2 * static_cast<size_t>(sms);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    prm.stream_k = 1;
+    prm.sk_unit0 = units - tail;
+    prm.ws_o = reinterpret_cast<float*>(base);
+    prm.ws_ml = reinterpret_cast<float*>(base + align256(slots * 2 * D * kBM * 4));
+    prm.ws_cnt = reinterpret_cast<unsigned int*>(base + align256(slots * 2 * D * kBM * 4) +
+                                                 align256(slots * 2 * 2 * kBM * 4));
+    cudaError_t me = cudaMemsetAsync(prm.ws_cnt, 0, static_cast<size_t>(sms) * 2 * 4, stream);
+    if (me != cudaSuccess) return attn_internal::cuda_status(me);
+  } else if (C::NQ == 2 && mode == ATTN_SCHEDULE_ONE_TILE) {
     prm.full_units = 0;  // every entry a half unit: one Q tile per CTA at a time
     prm.num_units = 2 * units;
   } else if (C::NQ == 2 && !prm.causal) {
@@ -854,7 +1096,7 @@ attn_status launch_fwd(const void* q, const void* k, const void* v, FwdParams pr
       prm.num_units = units + rest;
     }
   }
-  const int grid = prm.num_units < sms ? prm.num_units : sms;
+  const int grid = prm.stream_k ? sms : (prm.num_units < sms ? prm.num_units : sms);
   attn_fwd_kernel<D, KIND><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mo, prm);
   return attn_internal::cuda_status(cudaGetLastError());
 }

@@ -109,7 +109,8 @@ ATTN_EXPORT void attn_set_wait_timeout_ns(uint64_t timeout_ns) {
 }
 
 ATTN_EXPORT attn_status attn_set_schedule(int mode) {
-  if (mode != ATTN_SCHEDULE_PINGPONG && mode != ATTN_SCHEDULE_ONE_TILE) return ATTN_ERR_INVALID_ARG;
+  if (mode != ATTN_SCHEDULE_PINGPONG && mode != ATTN_SCHEDULE_ONE_TILE && mode != ATTN_SCHEDULE_BALANCED)
+    return ATTN_ERR_INVALID_ARG;
   g_schedule.store(mode);
   return ATTN_OK;
 }

@@ -90,6 +90,46 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
                      int N, int d, int causal, float scale, attn_dtype dtype, void* stream);
 
 /*
+ * attn_fwd_workspace_bytes -- workspace (bytes) that lets attn_fwd_ws and
+ * attn_fwd_fp8_ws balance full attention over the GPU's SMs, for head
+ * dimension d on the current device; 0 when d has no balanced schedule
+ * (d = 256, or a d this build does not take).  It depends only on d and the
+ * device's SM count (about 40 MiB at d = 128 on 152 SMs).
+ */
+size_t attn_fwd_workspace_bytes(int d);
+
+/*
+ * attn_fwd_ws -- attn_fwd with a caller-provided device workspace, used to
+ * balance the work over the SMs when it does not divide evenly.
+ *
+ * Work is scheduled per CTA (one per SM) in units of two 128-row query tiles
+ * of one head.  When the units do not divide evenly over the SMs, the last
+ * round leaves SMs idle while it costs a full unit.  With a workspace, full
+ * attention (causal = 0, d <= 128, at least one unit per SM) instead runs the
+ * whole rounds as before and cuts the (unit, key block) steps of the last
+ * units (at least half a round of them) into equal contiguous ranges, one
+ * per CTA (a stream-K tail): a unit cut between CTAs is computed in parts
+ * over disjoint key ranges, each writes its unnormalised O and its running
+ * maximum and sum to the workspace, and the part that finishes last merges
+ * them with the online-softmax rescaling and writes O and lse.  By default
+ * only the FP8 kernel takes the tail (see attn_set_schedule); results equal
+ * attn_fwd's up to the float32 summation order (FP8: up to the E4M3 rounding
+ * of each part's weights).  Causal attention and other shapes run exactly
+ * as attn_fwd.
+ *
+ *   workspace       : device buffer, 256-byte aligned (else ATTN_ERR_MISALIGNED),
+ *                     owned by the caller; NULL or fewer than
+ *                     attn_fwd_workspace_bytes(d) bytes = attn_fwd's schedule.
+ *                     The call zeroes the arrival counters in it on `stream`
+ *                     before the launch.  Calls whose GPU work overlaps must
+ *                     use different workspaces.
+ * Other arguments, rules and errors: attn_fwd.
+ */
+attn_status attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                        int N, int d, int causal, float scale, attn_dtype dtype, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/*
  * attn_fwd_ex -- attn_fwd generalised to Nq queries over Nk keys and to a
  * second memory layout.
  *
@@ -191,7 +231,7 @@ attn_status attn_fwd_host_noalloc(const void* q_host, const void* k_host, const 
  *                 unchanged); V is never rotated.
  *   per_tensor  : 0 = per-block scales (the FP8 method); 1 = one scale per
  *                 tensor (the naive FP8 baseline the pages compare against).
- *   d           : 128 (the FP8 path supports only this head dimension).
+ *   d           : 64, 128 or 256.
  * Quantisation: s = amax / 448 over the block (or tensor), 1 if amax = 0;
  * code = E4M3(x / s), division and rounding (nearest even, saturating to
  * +-448) in float32.  Asynchronous on `stream`.
@@ -241,7 +281,7 @@ attn_status attn_fp8_prepare_rotary(const void* q, const void* k, const void* v,
  *                the naive per-tensor FP8 baseline the pages compare against.
  *   o          : [B, H, N, d] device bf16, written.
  *   lse        : [B, H, N] device float32 or NULL.
- *   d          : 128.  Other arguments as for attn_fwd.
+ *   d          : 64, 128 or 256.  Other arguments as for attn_fwd.
  * Both products run on the FP8 tensor cores with float32 accumulation; the
  * softmax runs in float32 and P is rounded to E4M3 before P V.  When the
  * queries and keys were rotated by attn_fp8_prepare, O and lse are those of
@@ -251,6 +291,15 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const f
                          const float* k_scale, const float* v_scale, int per_tensor, void* o,
                          float* lse, int B, int H, int N, int d, int causal, float scale,
                          void* stream);
+
+/*
+ * attn_fwd_fp8_ws -- attn_fwd_fp8 with the balanced schedule of attn_fwd_ws
+ * (same workspace rules; the FP8 kernel's per-part O includes its V scale).
+ */
+attn_status attn_fwd_fp8_ws(const void* q8, const void* k8, const void* v8, const float* q_scale,
+                            const float* k_scale, const float* v_scale, int per_tensor, void* o,
+                            float* lse, int B, int H, int N, int d, int causal, float scale,
+                            void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * attn_get_device_status -- synchronises `stream`, then returns and clears the
@@ -275,10 +324,15 @@ void attn_set_wait_timeout_ns(uint64_t timeout_ns);
  *   ATTN_SCHEDULE_ONE_TILE: each CTA works on one Q tile at a time (the same
  *       kernel with the second tile idle), so softmax and products of a tile
  *       alternate without overlap.  Same results, bit for bit.
+ *   ATTN_SCHEDULE_BALANCED: ping-pong, and calls given a workspace
+ *       (attn_fwd_ws, attn_fwd_fp8_ws) take the stream-K tail for every
+ *       operand type.  By default only the FP8 kernel takes it: on the
+ *       benchmark shapes it measured faster there and slower for fp16/bf16.
  * Returns ATTN_ERR_INVALID_ARG for any other value (the mode is unchanged).
  */
 #define ATTN_SCHEDULE_PINGPONG 0
 #define ATTN_SCHEDULE_ONE_TILE 1
+#define ATTN_SCHEDULE_BALANCED 2
 attn_status attn_set_schedule(int mode);
 
 /*

@@ -26,6 +26,8 @@ def test_schedule_switch(lib):
     assert lib.attn_set_schedule(7) == attn.ATTN_ERR_INVALID_ARG
     assert lib.attn_set_schedule(-1) == attn.ATTN_ERR_INVALID_ARG
     assert lib.attn_set_schedule(attn.SCHEDULE_ONE_TILE) == attn.ATTN_OK
+    assert lib.attn_set_schedule(attn.SCHEDULE_BALANCED) == attn.ATTN_OK
+    assert lib.attn_set_schedule(3) == attn.ATTN_ERR_INVALID_ARG
     assert lib.attn_set_schedule(attn.SCHEDULE_PINGPONG) == attn.ATTN_OK
 
 

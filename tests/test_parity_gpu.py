@@ -283,3 +283,59 @@ def test_chunked_prefill_matches_full_causal():
     o_ref, l_ref = oracle.attention(q.cpu()[:, :1], k.cpu()[:, :1], v.cpu()[:, :1], causal=True, scale=d ** -0.5, rows=rows)
     m = parity.metrics(o_full[:, :1, rows], l_full[:, :1, rows], o_ref, l_ref)
     parity.assert_close(m, what="full causal sampled rows")
+
+
+# Stream-K schedule (attn_fwd_ws with a workspace): units = B * H * N / 256 two-tile
+# units over the SMs; shapes with units >= SMs and units % SMs != 0 cut most units
+# between two CTAs (for 160 units of 4-8 key blocks on 152 SMs, nearly every one).
+STREAM_K_CASES = [(4, 10, 1024, 128, "bf16"), (4, 10, 1000, 64, "fp16"), (2, 20, 1024, 64, "bf16"),
+                  (1, 33, 2048 + 77, 128, "bf16"), (2, 16, 8192, 128, "bf16")]
+
+
+@pytest.fixture
+def balanced_schedule():
+    """The 16-bit kernels take the stream-K tail only in this mode."""
+    attn.set_schedule(attn.SCHEDULE_BALANCED)
+    yield
+    attn.set_schedule(attn.SCHEDULE_PINGPONG)
+
+
+@pytest.mark.parametrize("case", STREAM_K_CASES)
+def test_stream_k_schedule_matches_oracle(case, balanced_schedule):
+    B, H, N, d, dt = case
+    q, k, v = parity.inputs(B, H, N, d, dt, seed=N + H)
+    ws = torch.empty(attn.workspace_bytes(d), dtype=torch.uint8, device="cuda")
+    assert ws.numel() > 0
+    scale = d ** -0.5
+    for causal in (False, True):  # causal takes the ordinary schedule
+        o, lse = attn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale, workspace=ws)
+        torch.cuda.synchronize()
+        assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())
+        rows = None if N <= 2100 else synth.sample_rows(N, 96, seed=1, salt=N)
+        o_ref, lse_ref = oracle.attention(q, k, v, causal=causal, scale=scale, rows=rows)
+        if rows is not None:
+            idx = torch.as_tensor(rows, device="cuda")
+            o, lse = o[:, :, idx], lse[:, :, idx]
+        parity.assert_close_elementwise(o.cpu(), lse.cpu(), o_ref, lse_ref, q, k, v, causal, scale, rows=rows,
+                                        what=f"stream-K {case} causal={causal}")
+        # and against the round-robin schedule of the same kernel
+        o2, lse2 = attn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale)
+        if rows is not None:
+            o2, lse2 = o2[:, :, idx], lse2[:, :, idx]
+        assert (o.float() - o2.float()).abs().max().item() <= 1e-2
+        assert (lse - lse2).abs().max().item() <= 1e-4
+    assert attn.device_status() == attn.ATTN_OK
+
+
+def test_stream_k_repeated_launches_reuse_the_workspace(balanced_schedule):
+    """Back-to-back launches on one workspace (the arrival counters are zeroed
+    on the stream before each launch): identical results every time."""
+    q, k, v = (t.cuda() for t in parity.inputs(4, 10, 1024, 128, "bf16", seed=3))
+    ws = torch.empty(attn.workspace_bytes(128), dtype=torch.uint8, device="cuda")
+    first, _ = attn.attn_fwd(q, k, v, workspace=ws)
+    first = first.clone()
+    for _ in range(5):
+        o, _ = attn.attn_fwd(q, k, v, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o, first)
+    assert attn.device_status() == attn.ATTN_OK
