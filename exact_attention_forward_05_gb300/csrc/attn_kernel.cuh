@@ -809,14 +809,23 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             tc_fence_after();
           }
           if (__any_sync(0xffffffffu, rescale)) {
+            // Up to 128 columns of O in flight under one wait (the registers
+            // that held S are free by now).
+            constexpr int GRP = D / 32 < 4 ? D / 32 : 4;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t o[32];
-              tmem_ld32(tm_o + 32 * c, o);
-              tmem_wait_ld(o);
+            for (int c0 = 0; c0 < D / 32; c0 += GRP) {
+              uint32_t o[GRP][32];
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-              tmem_st32(tm_o + 32 * c, o);
+              for (int g = 0; g < GRP; ++g) tmem_ld32(tm_o + 32 * (c0 + g), o[g]);
+              tmem_wait_ld(o[0]);
+#pragma unroll
+              for (int g = 1; g < GRP; ++g) reg_pin(o[g]);
+#pragma unroll
+              for (int g = 0; g < GRP; ++g) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[g][i] = __float_as_uint(__uint_as_float(o[g][i]) * alpha);
+                tmem_st32(tm_o + 32 * (c0 + g), o[g]);
+              }
             }
           }
         }
