@@ -754,6 +754,45 @@ def run_sweep(args):
         raise RuntimeError("device status after the sweep")
 
 
+def run_backward(args):
+    """Backward pass (attn_bwd: the row dot products D, the main kernel, the
+    final dQ pass) on the bench workload's shapes, causal and not, each line
+    at least 0.5 s of back-to-back calls with its clock record.  FLOPs:
+    2.5 x the forward's 4 B H N^2 d (five products per block pair against the
+    forward's two), halved when causal."""
+    import exact_attention_forward_05_gb300 as attn
+    import synth
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(0)
+    time.sleep(0.5)
+    w0 = WORKLOADS[args.workload]
+    B, H, N, d = w0["B"], w0["H"], w0["N"], w0["d"]
+    q, k, v = (t.to(dev) for t in synth.attention_inputs(B, H, N, d, "bf16", seed=0))
+    g = synth.attention_inputs(B, H, N, d, "bf16", seed=1000)[0].to(dev)
+    ws = torch.empty(attn.bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+    grads = tuple(torch.empty_like(q) for _ in range(3))
+    try:
+        for causal in (False, True):
+            o, lse = attn.attn_fwd(q, k, v, causal=causal)
+            f = lambda: attn.attn_bwd(q, k, v, o, g, lse, causal=causal, workspace=ws, out=grads, stream=stream)
+            for _ in range(max(args.warmup, 3)):
+                f()
+            ms, n, clocks = time_for(f, 0.5, stream, sampler)
+            w = dict(B=B, H=H, N=N, d=d, causal=causal, dtype="bf16")
+            fl = 2.5 * flops(w)
+            tf = fl / (ms * 1e-3) / 1e12
+            rl = roofline(tf)
+            print(json.dumps({"workload": "backward of " + describe(w), "value": round(tf, 1), "unit": UNIT,
+                              "flops_convention": "2.5 x 4 B H N^2 d (halved when causal)",
+                              "frac": rl["frac"], "frac_nominal": rl["frac_nominal"], "ms": round(ms, 4),
+                              "launches": n, "clocks": clocks}), flush=True)
+    finally:
+        sampler.stop()
+    if attn.device_status() != attn.ATTN_OK:
+        raise RuntimeError("device status after the backward")
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -765,9 +804,14 @@ def main():
                     help="overlap ablation: the bench workload under both work schedules, one line each")
     ap.add_argument("--sweep", action="store_true",
                     help="print one device-timed line per sweep configuration instead")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass on the workload's shapes (causal and not), one line each")
     args = ap.parse_args()
     if args.sweep:
         run_sweep(args)
+        return
+    if args.backward:
+        run_backward(args)
         return
     if args.ablation:
         run_ablation(args)

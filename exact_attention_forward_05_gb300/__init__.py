@@ -21,7 +21,7 @@ import torch
 
 from . import build as _build
 
-__all__ = ["attn_fwd", "workspace_bytes", "attn_fwd_host", "fp8_prepare", "attn_fwd_fp8", "attn_fwd_fp8_pipeline", "host_workspace_bytes", "device_status",
+__all__ = ["attn_fwd", "workspace_bytes", "attn_bwd", "bwd_workspace_bytes", "attn_fwd_host", "fp8_prepare", "attn_fwd_fp8", "attn_fwd_fp8_pipeline", "host_workspace_bytes", "device_status",
            "set_wait_timeout_ns", "set_schedule", "debug_bounded_wait", "debug_fail_host_chunk", "debug_exp2_poly",
            "attn_fwd_host_noalloc", "status_string", "library_path",
            "AttnError", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
@@ -95,6 +95,11 @@ def _load():
             lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
                                          i32, f32, vp]
             lib.attn_fwd_fp8.restype = i32
+            lib.attn_bwd_workspace_bytes.argtypes = [i32, i32, i32, i32]
+            lib.attn_bwd_workspace_bytes.restype = sz
+            lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32,
+                                     vp, sz, vp]
+            lib.attn_bwd.restype = i32
             lib.attn_get_device_status.argtypes = [vp]
             lib.attn_get_device_status.restype = i32
             lib.attn_set_wait_timeout_ns.argtypes = [u64]
@@ -363,6 +368,37 @@ def attn_fwd_fp8_pipeline(q, k, v, signs=None, causal: bool = False, scale: floa
     q8, k8, v8, qs, ks, vs = fp8_prepare(q, k, v, signs=signs, per_tensor=per_tensor, stream=stream,
                                          rope=rope, rope_interleaved=rope_interleaved)
     return attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=causal, scale=scale, stream=stream)
+
+
+def bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(_load().attn_bwd_workspace_bytes(B, H, N, d))
+
+
+def attn_bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
+             workspace: torch.Tensor | None = None, out=None, stream=None):
+    """Gradients (dQ, dK, dV) of attn_fwd for dL/dO = ``dout`` on CUDA tensors
+    [B, H, N, d] (d = 64 or 128, fp16 or bf16), given attn_fwd's ``o`` and
+    ``lse``; the softmax weights are recomputed from Q, K and lse.  ``out``
+    may pass (dq, dk, dv); ``workspace`` (uint8, bwd_workspace_bytes) is
+    allocated here when not given."""
+    B, H, N, d = _shape_of(q, k, v)
+    for t in (o, dout):
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous() or t.device != q.device:
+            raise ValueError("o and dout must be contiguous tensors like q")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = out if out is not None else (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    if workspace is None:
+        workspace = torch.empty(max(bwd_workspace_bytes(B, H, N, d), 1), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        st = _load().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                              lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+                              int(bool(causal)), float(scale), _DTYPES[q.dtype], workspace.data_ptr(),
+                              workspace.numel(), _stream_handle(stream, q.device))
+    _check(st, "attn_bwd")
+    return dq, dk, dv
 
 
 def device_status(stream=None) -> int:

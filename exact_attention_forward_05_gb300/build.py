@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libattn_gb300.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
-SOURCES = ["host_common.cu", "attn_fwd.cu", "attn_fp8.cu"]
+SOURCES = ["host_common.cu", "attn_fwd.cu", "attn_fp8.cu", "attn_bwd.cu"]
 HEADERS = ["sm103.cuh", "host_common.h", "attn_kernel.cuh", "tmap_cache.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

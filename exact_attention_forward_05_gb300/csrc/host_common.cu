@@ -98,10 +98,11 @@ using namespace attn_internal;
 ATTN_EXPORT attn_status attn_get_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_status(e);
-  unsigned int a = 0, b = 0;
+  unsigned int a = 0, b = 0, c = 0;
   if ((e = fwd_status_exchange(&a)) != cudaSuccess) return cuda_status(e);
   if ((e = fp8_status_exchange(&b)) != cudaSuccess) return cuda_status(e);
-  return (a | b) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+  if ((e = bwd_status_exchange(&c)) != cudaSuccess) return cuda_status(e);
+  return (a | b | c) ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }
 
 ATTN_EXPORT void attn_set_wait_timeout_ns(uint64_t timeout_ns) {

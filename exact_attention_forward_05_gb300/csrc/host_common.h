@@ -46,5 +46,6 @@ inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 // Per-module status exchange: read the module's device status word and clear it.
 cudaError_t fwd_status_exchange(unsigned int* out);
 cudaError_t fp8_status_exchange(unsigned int* out);
+cudaError_t bwd_status_exchange(unsigned int* out);
 
 }  // namespace attn_internal

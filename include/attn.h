@@ -302,6 +302,42 @@ attn_status attn_fwd_fp8_ws(const void* q8, const void* k8, const void* v8, cons
                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_bwd_workspace_bytes -- device workspace (bytes) attn_bwd needs: a float32
+ * dQ accumulator [B, H, N, d] and the row dot products D [B, H, N], each
+ * 256-byte aligned.  0 for a head dimension attn_bwd does not take.
+ */
+size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * attn_bwd -- backward pass of attn_fwd: dQ, dK, dV for a given dO = dL/dO.
+ * The softmax weights are recomputed block by block from Q, K and the
+ * forward's lse instead of being stored ("FlashAttention -- one, two,
+ * three!", section "FlashAttention v1.", the recomputation in the backward
+ * pass); lse is an auxiliary output, no gradient flows through it.  With
+ * P = exp(scale Q K^T - lse) (masked entries 0) and D = rowsum(dO o O):
+ *   dV = P^T dO,   dS = P o (dO V^T - D),   dQ = scale dS K,   dK = scale dS^T Q.
+ *
+ *   q, k, v, o, dout : [B, H, N, d] device, dtype `dtype`, read only; o and lse
+ *                      are attn_fwd's outputs for q, k, v (same causal, scale).
+ *   lse              : [B, H, N] device float32.
+ *   dq, dk, dv       : [B, H, N, d] device, dtype `dtype`, written (rounded to
+ *                      nearest even once, from float32 accumulation).
+ *   d                : 64 or 128 (else ATTN_ERR_UNSUPPORTED).
+ *   causal, scale    : as for attn_fwd.
+ *   workspace        : device, 256-byte aligned, at least
+ *                      attn_bwd_workspace_bytes(B, H, N, d) bytes, owned by the
+ *                      caller; the call clears what it uses.
+ * The products run on tcgen05 with float32 accumulation in tensor memory; P
+ * and dS are rounded to the input dtype before the products that take them.
+ * Asynchronous on `stream` (three kernels and one memset).  Errors as for
+ * attn_fwd; a NULL workspace or one that is too small: ATTN_ERR_INVALID_ARG.
+ */
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                     int causal, float scale, attn_dtype dtype, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/*
  * attn_get_device_status -- synchronises `stream`, then returns and clears the
  * device status word of every kernel module: ATTN_ERR_TIMEOUT if any kernel
  * recorded a timed-out wait since the last call, else ATTN_OK (ATTN_ERR_CUDA if
