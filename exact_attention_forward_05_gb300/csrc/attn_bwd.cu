@@ -24,8 +24,11 @@
 //                       dV += P^T dO and dK += dS^T Q accumulate in TMEM;
 //                       dQ_i = dS K (queries on the TMEM lanes, so dS is read
 //                       from shared memory as an M-major operand) lands in
-//                       the S^T columns and is added to a float32 dQ
-//                       accumulator; at the end of the unit dV and scale dK
+//                       the S^T columns and is reduce-added (bulk tensor
+//                       reduce from shared memory) into a float32 dQ
+//                       accumulator; Q_i and dO_i are double-buffered so the
+//                       next block loads during this one; at the end of the
+//                       unit dV and scale dK
 //                       are rounded and stored;
 //   bwd_dq_kernel       dQ = scale * accumulator, rounded to the input type.
 #include <cuda_bf16.h>
@@ -55,19 +58,35 @@ __host__ __device__ constexpr uint32_t idesc(uint32_t fmt, int M, int N, uint32_
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// 4-D tiled reduce-add (float32 add into global memory) from shared memory,
+// bulk-group completion; elements of the box outside the tensor are skipped.
+__device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* map, uint32_t src, int x, int y, int z, int w) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
 template <int D>
 struct BCfg {
   static constexpr int CHUNK_BYTES = kB * 128;  // 128 rows x one 128-byte swizzle span (64 elements)
   static constexpr int CHUNKS = D * 2 / 128;
   static constexpr int TILE_BYTES = CHUNKS * CHUNK_BYTES;
-  static constexpr int DS_BYTES = 2 * CHUNK_BYTES;  // dS: 128 key rows x 128 queries, two 64-query spans
-  static constexpr int OFF_K = 0, OFF_V = TILE_BYTES, OFF_Q = 2 * TILE_BYTES, OFF_DO = 3 * TILE_BYTES;
-  static constexpr int OFF_DS = 4 * TILE_BYTES;
+  static constexpr int QD_STAGES = 2;               // Q_i, dO_i double-buffered
+  // dS: 128 key rows x 128 queries, two 64-query spans; after the dQ product
+  // has read it, the same bytes stage 64 float32 columns of the dQ partial
+  // (two 32-column, 128-byte swizzled boxes) for the reduce-add into dQ.
+  static constexpr int DS_BYTES = 2 * CHUNK_BYTES;
+  static constexpr int OFF_K = 0, OFF_V = TILE_BYTES;
+  static constexpr int OFF_Q = 2 * TILE_BYTES;                        // + stage * 2 * TILE_BYTES
+  static constexpr int OFF_DO = 3 * TILE_BYTES;                       // + stage * 2 * TILE_BYTES
+  static constexpr int OFF_DS = (2 + 2 * QD_STAGES) * TILE_BYTES;
   static constexpr int OFF_LSE = OFF_DS + DS_BYTES;  // 128 floats: lse * log2(e) of the query block
   static constexpr int OFF_D = OFF_LSE + 512;        // 128 floats: D of the query block
   static constexpr int OFF_BAR = OFF_D + 512;
-  enum : int { B_KV_FULL = 0, B_KV_EMPTY, B_QD_FULL, B_QD_EMPTY, B_SP_FULL, B_P_READY, B_DQ_FULL, B_DQ_READ,
-               B_EPI_DONE, B_MMA_DONE, NBARS };
+  enum : int { B_KV_FULL = 0, B_KV_EMPTY, B_QD_FULL, B_QD_EMPTY = B_QD_FULL + QD_STAGES,
+               B_SP_FULL = B_QD_EMPTY + QD_STAGES, B_P_READY, B_DQ_FULL, B_DQ_READ, B_EPI_DONE, B_MMA_DONE, NBARS };
   static constexpr int USED = OFF_BAR + 8 * NBARS + 16 + 1024;
   // One CTA per SM (TMEM is allocated whole): at least 115 KiB of shared memory.
   static constexpr int SMEM_BYTES = USED > 115 * 1024 ? USED : 115 * 1024;
@@ -133,13 +152,14 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                    const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using C = BCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
-  const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
+  auto sQ = [&](uint32_t st) { return smem_u32(smem + C::OFF_Q + st * 2 * C::TILE_BYTES); };
+  auto sDO = [&](uint32_t st) { return smem_u32(smem + C::OFF_DO + st * 2 * C::TILE_BYTES); };
   const uint32_t sDS = smem_u32(smem + C::OFF_DS);
   float* lse_s = reinterpret_cast<float*>(smem + C::OFF_LSE);
   float* d_s = reinterpret_cast<float*>(smem + C::OFF_D);
@@ -165,6 +185,7 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
     tma_prefetch(&tmK);
     tma_prefetch(&tmV);
     tma_prefetch(&tmDO);
+    tma_prefetch(&tmDQ);
   }
   tc_fence_before();
   __syncthreads();
@@ -194,16 +215,20 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
         load_tile(sK, &tmK, BAR(C::B_KV_FULL), j * kB, bh);
         load_tile(sV, &tmV, BAR(C::B_KV_FULL), j * kB, bh);
         for (int i = p.causal ? j : 0; ok && i < p.nkb; ++i) {
-          if (!(ok = mbar_wait(BAR(C::B_QD_EMPTY), (qd_it & 1u) ^ 1u, wc, attn_internal::kStatusTimeoutLoad))) break;
+          const uint32_t st = qd_it % C::QD_STAGES, ph = (qd_it / C::QD_STAGES) & 1u;
+          if (!(ok = mbar_wait(BAR(C::B_QD_EMPTY + st), ph ^ 1u, wc, attn_internal::kStatusTimeoutLoad))) break;
           ++qd_it;
-          mbar_arrive_expect_tx(BAR(C::B_QD_FULL), 2 * C::TILE_BYTES);
-          load_tile(sQ, &tmQ, BAR(C::B_QD_FULL), i * kB, bh);
-          load_tile(sDO, &tmDO, BAR(C::B_QD_FULL), i * kB, bh);
+          mbar_arrive_expect_tx(BAR(C::B_QD_FULL + st), 2 * C::TILE_BYTES);
+          load_tile(sQ(st), &tmQ, BAR(C::B_QD_FULL + st), i * kB, bh);
+          load_tile(sDO(st), &tmDO, BAR(C::B_QD_FULL + st), i * kB, bh);
         }
       }
       // No copies in flight when the CTA leaves.
       if (kv_it > 0) drain(BAR(C::B_KV_FULL), (kv_it - 1) & 1u, 100000000ull);
-      if (qd_it > 0) drain(BAR(C::B_QD_FULL), (qd_it - 1) & 1u, 100000000ull);
+      for (uint32_t k2 = 0; k2 < C::QD_STAGES && k2 < qd_it; ++k2) {
+        const uint32_t f = qd_it - 1 - k2;
+        drain(BAR(C::B_QD_FULL + f % C::QD_STAGES), (f / C::QD_STAGES) & 1u, 100000000ull);
+      }
     }
   } else if (warp == C::MMA_WARP) {
     // ---------------------------------------------------------- MMA issuer
@@ -243,7 +268,10 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
         tc_fence_after();
         const int i0 = p.causal ? j : 0;
         for (int i = i0; i < p.nkb; ++i) {
-          if (!(ok = mbar_wait(BAR(C::B_QD_FULL), qd_it & 1u, wc, attn_internal::kStatusTimeoutMma))) break;
+          const uint32_t st = qd_it % C::QD_STAGES;
+          if (!(ok = mbar_wait(BAR(C::B_QD_FULL + st), (qd_it / C::QD_STAGES) & 1u, wc,
+                               attn_internal::kStatusTimeoutMma)))
+            break;
           ++qd_it;
           if (!first_block) {  // the previous dQ partial has left the S^T columns
             if (!(ok = mbar_wait(BAR(C::B_DQ_READ), dqr_it & 1u, wc, attn_internal::kStatusTimeoutMma))) break;
@@ -251,8 +279,8 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
           }
           first_block = false;
           tc_fence_after();
-          mma_kmajor(tmem + C::TM_S, sK, sQ);    // S^T = K Q^T
-          mma_kmajor(tmem + C::TM_DP, sV, sDO);  // dP^T = V dO^T
+          mma_kmajor(tmem + C::TM_S, sK, sQ(st));    // S^T = K Q^T
+          mma_kmajor(tmem + C::TM_DP, sV, sDO(st));  // dP^T = V dO^T
           mma_commit(BAR(C::B_SP_FULL));
           if (!(ok = mbar_wait(BAR(C::B_P_READY), pr_it & 1u, wc, attn_internal::kStatusTimeoutMma))) break;
           ++pr_it;
@@ -261,8 +289,8 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
             ++epi_it;
           }
           tc_fence_after();
-          mma_tmem_a(tmem + C::TM_DV, tmem + C::TM_S, sDO, i > i0);   // dV += P^T dO
-          mma_tmem_a(tmem + C::TM_DK, tmem + C::TM_DP, sQ, i > i0);   // dK += dS^T Q
+          mma_tmem_a(tmem + C::TM_DV, tmem + C::TM_S, sDO(st), i > i0);   // dV += P^T dO
+          mma_tmem_a(tmem + C::TM_DK, tmem + C::TM_DP, sQ(st), i > i0);   // dK += dS^T Q
           {  // dQ_i = dS K into the S^T columns (after the products above read P^T)
             const uint32_t a0 = desc_sw128_lo(sDS, C::CHUNK_BYTES), b0 = desc_sw128_lo(sK, C::CHUNK_BYTES);
 #pragma unroll
@@ -271,7 +299,7 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
               mma_ss_w(tmem + C::TM_S, a0 + off, HI, b0 + off, HI, ID_DQ, kk > 0 ? 1u : 0u, false);
             }
           }
-          mma_commit(BAR(C::B_QD_EMPTY));
+          mma_commit(BAR(C::B_QD_EMPTY + st));
           mma_commit(BAR(C::B_DQ_FULL));
         }
         if (!ok) break;
@@ -297,7 +325,9 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
       const size_t head = static_cast<size_t>(bh) * p.N;
       for (int i = p.causal ? j : 0; i < p.nkb; ++i) {
         // This query block's lse (log2 units; +inf past N, so that P = 0
-        // there) and D, staged for the four warps.
+        // there) and D, staged for the four warps.  The dS buffer below is
+        // also the staging of the last dQ reduce: it must have been read.
+        if (threadIdx.x == 0) bulk_wait_read_all();
         if (bar_red_or(1, 128, !ok)) { ok = false; break; }
         const int q_row = i * kB + row;
         lse_s[row] = q_row < p.N ? p.lse[head + q_row] * kLog2e : INFINITY;
@@ -310,37 +340,52 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
         ++sp_it;
         tc_fence_after();
         const bool diag = p.causal && i == j;
+        // 64 queries at a time: S^T and dP^T columns of two 32-query chunks
+        // loaded under one wait; lse and D read four at a time.
 #pragma unroll 1
-        for (int c = 0; c < kB / 32; ++c) {
-          uint32_t s[32], dp[32];
-          tmem_ld32(lane_base + C::TM_S + 32 * c, s);
-          tmem_ld32(lane_base + C::TM_DP + 32 * c, dp);
-          tmem_wait_ld(s);
-          reg_pin(dp);
-          uint32_t pk[16], dk16[16];
+        for (int c2 = 0; c2 < kB / 64; ++c2) {
+          uint32_t s[2][32], dp[2][32];
+          tmem_ld32(lane_base + C::TM_S + 64 * c2, s[0]);
+          tmem_ld32(lane_base + C::TM_S + 64 * c2 + 32, s[1]);
+          tmem_ld32(lane_base + C::TM_DP + 64 * c2, dp[0]);
+          tmem_ld32(lane_base + C::TM_DP + 64 * c2 + 32, dp[1]);
+          tmem_wait_ld(s[0]);
+          reg_pin(s[1]);
+          reg_pin(dp[0]);
+          reg_pin(dp[1]);
 #pragma unroll
-          for (int t = 0; t < 32; t += 2) {
-            const int qc = 32 * c + t;
-            float p0 = ex2(p.sl2 * __uint_as_float(s[t]) - lse_s[qc]);
-            float p1 = ex2(p.sl2 * __uint_as_float(s[t + 1]) - lse_s[qc + 1]);
-            if (diag) {  // key row > query: masked
-              if (row > qc) p0 = 0.f;
-              if (row > qc + 1) p1 = 0.f;
+          for (int h = 0; h < 2; ++h) {
+            const int c = 2 * c2 + h;  // 32-query chunk
+            uint32_t pk[16], dk16[16];
+#pragma unroll
+            for (int t4 = 0; t4 < 8; ++t4) {
+              const int qc = 32 * c + 4 * t4;
+              const float4 l4 = *reinterpret_cast<const float4*>(lse_s + qc);
+              const float4 d4 = *reinterpret_cast<const float4*>(d_s + qc);
+              const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+              float pv[4], dsv[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float pe = ex2(p.sl2 * __uint_as_float(s[h][4 * t4 + e]) - lv[e]);
+                if (diag && row > qc + e) pe = 0.f;  // key row > query: masked
+                pv[e] = pe;
+                dsv[e] = pe * (__uint_as_float(dp[h][4 * t4 + e]) - dv4[e]);
+              }
+              pk[2 * t4] = pack16<BF16>(pv[0], pv[1]);
+              pk[2 * t4 + 1] = pack16<BF16>(pv[2], pv[3]);
+              dk16[2 * t4] = pack16<BF16>(dsv[0], dsv[1]);
+              dk16[2 * t4 + 1] = pack16<BF16>(dsv[2], dsv[3]);
             }
-            const float ds0 = p0 * (__uint_as_float(dp[t]) - d_s[qc]);
-            const float ds1 = p1 * (__uint_as_float(dp[t + 1]) - d_s[qc + 1]);
-            pk[t / 2] = pack16<BF16>(p0, p1);
-            dk16[t / 2] = pack16<BF16>(ds0, ds1);
-          }
-          tmem_st16(lane_base + C::TM_S + 16 * c, pk);
-          tmem_st16(lane_base + C::TM_DP + 16 * c, dk16);
-          // dS into shared memory: row `row`, queries 32c .. 32c + 31, 128-byte
-          // swizzled spans of 64 queries (the layout a tiled copy would give).
-          const uint32_t span = sDS + static_cast<uint32_t>(c >> 1) * C::CHUNK_BYTES + static_cast<uint32_t>(row) * 128u;
+            tmem_st16(lane_base + C::TM_S + 16 * c, pk);
+            tmem_st16(lane_base + C::TM_DP + 16 * c, dk16);
+            // dS into shared memory: row `row`, queries 32c .. 32c + 31, 128-byte
+            // swizzled spans of 64 queries (the layout a tiled copy would give).
+            const uint32_t span = sDS + static_cast<uint32_t>(c >> 1) * C::CHUNK_BYTES + static_cast<uint32_t>(row) * 128u;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const uint32_t unit = static_cast<uint32_t>((c & 1) * 4 + v) ^ static_cast<uint32_t>(row & 7);
-            st_shared_v4(span + (unit << 4), dk16[4 * v], dk16[4 * v + 1], dk16[4 * v + 2], dk16[4 * v + 3]);
+            for (int v = 0; v < 4; ++v) {
+              const uint32_t unit = static_cast<uint32_t>((c & 1) * 4 + v) ^ static_cast<uint32_t>(row & 7);
+              st_shared_v4(span + (unit << 4), dk16[4 * v], dk16[4 * v + 1], dk16[4 * v + 2], dk16[4 * v + 3]);
+            }
           }
         }
         tmem_wait_st();
@@ -353,17 +398,34 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
         if (bar_red_or(2, 128, !got)) { ok = false; break; }
         ++dq_it;
         tc_fence_after();
-        float4* dq_row = reinterpret_cast<float4*>(p.dq_acc + (head + q_row) * D);
+        // 64 columns at a time through the dS buffer (free: the dQ product
+        // has read it), two 32-float 128-byte swizzled boxes, reduce-added
+        // into the float32 accumulator (rows past N are skipped by the copy).
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(lane_base + C::TM_S + 32 * c, v);
-          tmem_wait_ld(v);
-          if (q_row < p.N) {
+        for (int rnd = 0; rnd < D / 64; ++rnd) {
+          uint32_t v[2][32];
+          tmem_ld32(lane_base + C::TM_S + 64 * rnd, v[0]);
+          tmem_ld32(lane_base + C::TM_S + 64 * rnd + 32, v[1]);
+          tmem_wait_ld(v[0]);
+          reg_pin(v[1]);
+          if (rnd > 0) {
+            if (threadIdx.x == 0) bulk_wait_read_all();
+            bar_sync_n(1, 128);
+          }
 #pragma unroll
-            for (int t = 0; t < 8; ++t)
-              atomicAdd(dq_row + 8 * c + t, make_float4(__uint_as_float(v[4 * t]), __uint_as_float(v[4 * t + 1]),
-                                                          __uint_as_float(v[4 * t + 2]), __uint_as_float(v[4 * t + 3])));
+          for (int b = 0; b < 2; ++b) {
+            const uint32_t box_row = sDS + static_cast<uint32_t>(b) * C::CHUNK_BYTES + static_cast<uint32_t>(row) * 128u;
+#pragma unroll
+            for (int u4 = 0; u4 < 8; ++u4)
+              st_shared_v4(box_row + ((static_cast<uint32_t>(u4) ^ static_cast<uint32_t>(row & 7)) << 4),
+                           v[b][4 * u4], v[b][4 * u4 + 1], v[b][4 * u4 + 2], v[b][4 * u4 + 3]);
+          }
+          fence_proxy_async_smem();
+          bar_sync_n(1, 128);
+          if (threadIdx.x == 0) {
+            tma_reduce_add_4d(&tmDQ, sDS, 64 * rnd, i * kB, bh, 0);
+            tma_reduce_add_4d(&tmDQ, sDS + C::CHUNK_BYTES, 64 * rnd + 32, i * kB, bh, 0);
+            bulk_commit_group();
           }
         }
         tc_fence_before();
@@ -406,6 +468,8 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
     }
   }
 
+  // The reduce-adds of dQ must finish before the CTA exits.
+  if (threadIdx.x == 0) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == C::MMA_WARP) {
@@ -476,6 +540,15 @@ attn_status run(const void* q, const void* k, const void* v, const void* o, cons
     return attn_internal::encode_tmap_4d(m, dt, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
   };
   if (!encode(&mq, q) || !encode(&mk, k) || !encode(&mv, v) || !encode(&mdo, dout)) return ATTN_ERR_CUDA;
+  CUtensorMap mdq;  // float32 accumulator [BH, N, d], box 32 floats x 128 rows
+  {
+    const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(N), static_cast<uint64_t>(BH), 1};
+    const uint64_t strides[3] = {D * 4ull, static_cast<uint64_t>(N) * D * 4, static_cast<uint64_t>(BH) * N * D * 4};
+    const uint32_t box[4] = {32, kB, 1, 1};
+    if (!attn_internal::encode_tmap_4d(&mdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dq_acc, dims, strides, box,
+                                       CU_TENSOR_MAP_SWIZZLE_128B))
+      return ATTN_ERR_CUDA;
+  }
 
   static std::mutex mu;
   static int configured[64] = {0};
@@ -508,7 +581,7 @@ attn_status run(const void* q, const void* k, const void* v, const void* o, cons
   const int sms = attn_internal::sm_count();
   if (sms <= 0) return ATTN_ERR_CUDA;
   const int grid = prm.num_units < sms ? prm.num_units : sms;
-  attn_bwd_kernel<D, BF16><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(mq, mk, mv, mdo, prm);
+  attn_bwd_kernel<D, BF16><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(mq, mk, mv, mdo, mdq, prm);
   if ((e = cudaGetLastError()) != cudaSuccess) return attn_internal::cuda_status(e);
   const int64_t n4 = static_cast<int64_t>(rows) * D / 4;
   bwd_dq_kernel<BF16><<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, s>>>(
