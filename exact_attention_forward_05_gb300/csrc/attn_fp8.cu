@@ -175,13 +175,29 @@ __global__ void __launch_bounds__(kPrepThreads, D <= 128 ? 2 : 1) fp8_prepare_ke
 
   const int row = blk * kQuantRows + warp * 8 + (lane >> 2);
   const bool have = row < p.N;
+  // Without a rotary embedding the signs go on the 16-bit input words, before
+  // the conversion (a sign-bit XOR commutes with it): per pair of values one
+  // byte permute moves the two sign bytes under bits 15 and 31 and one logic
+  // op applies them (block-uniform choice).
+  const bool pre_signs = qk && p.signs != nullptr && p.rcos == nullptr;
+  const int4* sgn = reinterpret_cast<const int4*>(p.signs + (bh % p.H) * D + VPL * g);
   float x[VPL];
   if (have) {
     const uint4* ptr = reinterpret_cast<const uint4*>(src + (head + static_cast<size_t>(row) * D + VPL * g) * 2);
 #pragma unroll
     for (int v = 0; v < VPL / 8; ++v) {
       const uint4 r = ptr[v];
-      const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+      uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+      if (pre_signs) {
+        // Sign bytes of elements 8v .. 8v + 7: two words of the 16-byte load v / 2.
+        const int4 sv = sgn[v >> 1];
+        const uint32_t s0 = static_cast<uint32_t>((v & 1) ? sv.z : sv.x);
+        const uint32_t s1 = static_cast<uint32_t>((v & 1) ? sv.w : sv.y);
+        w4[0] ^= __byte_perm(s0, 0u, 0x1404u) & 0x80008000u;
+        w4[1] ^= __byte_perm(s0, 0u, 0x3424u) & 0x80008000u;
+        w4[2] ^= __byte_perm(s1, 0u, 0x1404u) & 0x80008000u;
+        w4[3] ^= __byte_perm(s1, 0u, 0x3424u) & 0x80008000u;
+      }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         float2 f;
@@ -203,10 +219,11 @@ __global__ void __launch_bounds__(kPrepThreads, D <= 128 ? 2 : 1) fp8_prepare_ke
     rotary_row<VPL>(x, g, cr, sr, p.rope_interleaved != 0, have);
   }
   if (qk && p.signs != nullptr) {
-    // Signs (+1 = 0x01, -1 = 0xff): bit 7 of each byte becomes the float's sign bit.
-    const int4* sp = reinterpret_cast<const int4*>(p.signs + (bh % p.H) * D + VPL * g);
+    // Signs (+1 = 0x01, -1 = 0xff): bit 7 of each byte becomes the float's sign
+    // bit (here only after a rotary embedding; otherwise applied above).
+    const int4* sp = sgn;
 #pragma unroll
-    for (int v = 0; v < VPL / 16; ++v) {
+    for (int v = 0; v < VPL / 16 && !pre_signs; ++v) {
       const int4 sv = sp[v];
       const uint32_t sw[4] = {static_cast<uint32_t>(sv.x), static_cast<uint32_t>(sv.y),
                               static_cast<uint32_t>(sv.z), static_cast<uint32_t>(sv.w)};
