@@ -323,16 +323,27 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
       decode(u, p, bh, j);
       const int key = j * kB + row;
       const size_t head = static_cast<size_t>(bh) * p.N;
-      for (int i = p.causal ? j : 0; i < p.nkb; ++i) {
-        // This query block's lse (log2 units; +inf past N, so that P = 0
-        // there) and D, staged for the four warps.  The dS buffer below is
-        // also the staging of the last dQ reduce: it must have been read.
+      const int i0 = p.causal ? j : 0;
+      // lse (log2 units; +inf past N, so that P = 0 there) and D of this
+      // thread's row of the next query block, loaded one block ahead.
+      auto fetch = [&](int i, float& l2, float& dd) {
+        const int q = i * kB + row;
+        const bool in = i < p.nkb && q < p.N;
+        l2 = in ? p.lse[head + q] * kLog2e : INFINITY;
+        dd = in ? p.dvec[head + q] : 0.f;
+      };
+      float next_l2, next_d;
+      fetch(i0, next_l2, next_d);
+      for (int i = i0; i < p.nkb; ++i) {
+        // Stage this block's values for the four warps.  The dS buffer below
+        // is also the staging of the last dQ reduce: it must have been read.
         if (threadIdx.x == 0) bulk_wait_read_all();
         if (bar_red_or(1, 128, !ok)) { ok = false; break; }
         const int q_row = i * kB + row;
-        lse_s[row] = q_row < p.N ? p.lse[head + q_row] * kLog2e : INFINITY;
-        d_s[row] = q_row < p.N ? p.dvec[head + q_row] : 0.f;
+        lse_s[row] = next_l2;
+        d_s[row] = next_d;
         bar_sync_n(1, 128);
+        fetch(i + 1, next_l2, next_d);
         if (!(ok = mbar_wait_warp(BAR(C::B_SP_FULL), sp_it & 1u, wc, attn_internal::kStatusTimeoutSoftmax))) {
           bar_red_or(2, 128, true);
           break;
