@@ -232,3 +232,29 @@ def test_header_is_plain_c(tmp_path):
                    f'int main(void) {{ return (int)(sizeof fns / sizeof fns[0]) - {len(names)}; }}\n')
     subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", inc, "-c", str(src),
                     "-o", str(tmp_path / "use_header.o")], check=True)
+
+
+def test_bwd_validation_before_launch(lib):
+    """attn_bwd rejects bad arguments before any CUDA work (fake addresses are
+    never dereferenced); an empty problem returns ATTN_OK without a launch."""
+    def bwd(d=128, N=64, dtype=attn.ATTN_BF16, ws=0x10000, ws_bytes=1 << 30, scale=0.1, **kw):
+        a = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, g=0x5000, lse=0x6000, dq=0x7000, dk=0x8000,
+                 dv=0x9000)
+        a.update(kw)
+        return lib.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["g"], a["lse"], a["dq"], a["dk"], a["dv"], 1, 2,
+                            N, d, 0, scale, dtype, ws, ws_bytes, None)
+    for bad_d in (32, 96, 256):
+        assert bwd(d=bad_d) == attn.ATTN_ERR_UNSUPPORTED
+    assert bwd(dtype=5) == attn.ATTN_ERR_UNSUPPORTED
+    assert bwd(scale=float("nan")) == attn.ATTN_ERR_INVALID_ARG
+    assert bwd(q=None) == attn.ATTN_ERR_INVALID_ARG
+    assert bwd(lse=None) == attn.ATTN_ERR_INVALID_ARG
+    assert bwd(ws=None) == attn.ATTN_ERR_INVALID_ARG
+    assert bwd(ws_bytes=16) == attn.ATTN_ERR_INVALID_ARG
+    assert bwd(dq=0x7008) == attn.ATTN_ERR_MISALIGNED
+    assert bwd(ws=0x10010) == attn.ATTN_ERR_MISALIGNED
+    assert bwd(lse=0x6002) == attn.ATTN_ERR_MISALIGNED
+    assert bwd(N=0) == attn.ATTN_OK
+    assert bwd(N=-1) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_bwd_workspace_bytes(1, 2, 64, 128) == 1 * 2 * 64 * 128 * 4 + 512
+    assert lib.attn_bwd_workspace_bytes(1, 2, 64, 96) == 0
