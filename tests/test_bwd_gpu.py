@@ -3,7 +3,7 @@ oracle's gradients (oracle.attention_bwd, the chain rule through the
 definition), every element, on the same rounded inputs and dO.  O and lse come
 from the forward kernel.
 
-Tolerance (derived from the arithmetic, design reading 13): each gradient is
+Tolerance (derived from the arithmetic; the pages fix none for gradients): each gradient is
 rounded once to the 16-bit type at the end (relative error up to u, RMS about
 u / sqrt(3) for uniformly spread rounding), and P, dS and O (inside D) carry one
 rounding each into float32 sums whose terms mostly do not cancel.  Checked per
