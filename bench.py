@@ -316,17 +316,6 @@ def traffic_from_profile():
     return prof.get("dram_bytes_per_launch_full_workload")
 
 
-def sampled_parity(o, lse, q, k, v, w, rows):
-    import oracle  # test infrastructure: parity check outside the timed region
-    o_ref, lse_ref = oracle.attention(q[:1, :1], k[:1, :1], v[:1, :1], causal=w["causal"],
-                                      scale=w["d"] ** -0.5, rows=rows)
-    idx = torch.as_tensor(rows)
-    og = o[:1, :1, idx].double().cpu().numpy()
-    lg = lse[:1, :1, idx].double().cpu().numpy()
-    return {"rows": len(rows), "max_abs": float(np.abs(og - o_ref).max()),
-            "lse_abs": float(np.abs(lg - lse_ref).max())}
-
-
 def cpu_baseline(w, q, k, v, budget_s: float = 12.0):
     """The oracle as it stands, on every host core, on a bounded sample of the
     workload: whole heads (all their query rows) when one head fits the time
@@ -445,8 +434,6 @@ def run_gpu(args):
     achieved = flops(w) / (ms / args.steps * 1e-3) / 1e12
     line = None
     if rank == 0:
-        rows = synth.sample_rows(N, 16, seed=0, salt=7)
-        par = sampled_parity(o.cpu(), lse.cpu(), q, k, v, w, rows)
         cpu = cpu_baseline(w, q, k, v)
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -476,7 +463,6 @@ def run_gpu(args):
                            "clocks": clocks_o},
             "fp8": fp8,
             "host": host,
-            "parity_sample": par,
             "device": torch.cuda.get_device_name(dev),
         }
     if world > 1:
@@ -582,21 +568,15 @@ def fp8_leg(w, dev, stream, rank, args, sampler=None):
                                 "algorithmic_bytes": prep_bytes, "clocks": clocks_prep},
            "pipeline_value": round(fl / (t_both * 1e-3) / 1e12, 2)}
     if rank == 0:
-        import oracle
-        rows = synth.sample_rows(N, 16, seed=0, salt=11)
-        idx = torch.as_tensor(rows, device=dev)
-        ob, _ = attn.attn_fwd_fp8_pipeline(qd, kd, vd, signs=None, causal=w["causal"], scale=scale,
+        # Accuracy beside the rate, outside the timed region: RMS of the FP8 output against the
+        # bf16 kernel's on the same inputs, every element (parity against the float64 oracle is
+        # the tests' job).
+        ob = attn.attn_fwd(qd, kd, vd, causal=w["causal"], scale=scale)[0].float()
+        on, _ = attn.attn_fwd_fp8_pipeline(qd, kd, vd, signs=None, causal=w["causal"], scale=scale,
                                            per_tensor=True)
-        e8, eb = [], []
-        for h in (0, B * H - 1):
-            bsel, hsel = divmod(h, H)
-            sl = (slice(bsel, bsel + 1), slice(hsel, hsel + 1))
-            o_ref, _ = oracle.attention(q[sl], k[sl], v[sl], causal=w["causal"], scale=scale, rows=rows)
-            e8.append(o8[sl][:, :, idx].double().cpu().numpy() - o_ref)
-            eb.append(ob[sl][:, :, idx].double().cpu().numpy() - o_ref)
-        out["rms"] = float(np.sqrt(np.mean(np.concatenate(e8) ** 2)))
-        out["rms_naive_per_tensor"] = float(np.sqrt(np.mean(np.concatenate(eb) ** 2)))
-        out["rms_rows"] = f"{len(rows)} rows x 2 heads"
+        out["rms_vs_bf16_kernel"] = float((o8.float() - ob).square().mean().sqrt())
+        out["rms_vs_bf16_kernel_naive_per_tensor"] = float((on.float() - ob).square().mean().sqrt())
+        del ob, on
     return out
 
 
