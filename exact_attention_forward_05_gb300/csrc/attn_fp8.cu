@@ -51,13 +51,16 @@ struct PrepParams {
 // Correctly rounded x / s from y = RN(1 / s) with one FMA correction of the
 // product (Markstein, "Computation of elementary functions on the IBM RISC
 // System/6000 processor", IBM J. Res. Dev. 34(1), 1990): q0 = RN(x y),
-// r = x - s q0 exactly, q = RN(q0 + r y).  Used where |x / s| <= 448 and s is
-// a normal number far from the exponent limits; other scales take the
-// division itself.  Two quotients at a time: ns2 = (-s, -s), y2 = (y, y).
-__device__ __forceinline__ float2 div_by_scale2(float2 x, float2 ns2, float2 y2) {
+// e = q0 s - x exactly, q = RN(q0 - e y).  The residual is taken as q0 s - x
+// (not x - q0 s) so that a zero keeps its sign: x = -0 gives e = +0 and
+// q = RN(-0 + -0) = -0, where RN(q0 + r y) with r = x - q0 s gives +0.  Used
+// where |x / s| <= 448 and s is a normal number far from the exponent limits;
+// other scales take the division itself.  Two quotients at a time:
+// s2 = (s, s), ny2 = (-y, -y), y2 = (y, y).
+__device__ __forceinline__ float2 div_by_scale2(float2 x, float2 s2, float2 ny2, float2 y2) {
   const float2 q0 = fmul2(x, y2);
-  const float2 r = ffma2(q0, ns2, x);
-  return ffma2(r, y2, q0);
+  const float2 e = ffma2(q0, s2, fmul2(x, make_float2(-1.f, -1.f)));
+  return ffma2(e, ny2, q0);
 }
 
 template <int VPL>
@@ -270,13 +273,13 @@ __global__ void __launch_bounds__(kPrepThreads, D <= 128 ? 2 : 1) fp8_prepare_ke
     const float y = __frcp_rn(s);
     if (have) {
       uint32_t pk[VPL / 4];
-      const float2 ns2 = make_float2(-s, -s), y2 = make_float2(y, y);
+      const float2 s2 = make_float2(s, s), ny2 = make_float2(-y, -y), y2 = make_float2(y, y);
 #pragma unroll
       for (int k = 0; k < VPL / 4; ++k) {
         float2 q01, q23;
         if (fast) {
-          q01 = div_by_scale2(pair(x, 4 * k), ns2, y2);
-          q23 = div_by_scale2(pair(x, 4 * k + 2), ns2, y2);
+          q01 = div_by_scale2(pair(x, 4 * k), s2, ny2, y2);
+          q23 = div_by_scale2(pair(x, 4 * k + 2), s2, ny2, y2);
         } else {
           q01 = make_float2(__fdiv_rn(x[4 * k], s), __fdiv_rn(x[4 * k + 1], s));
           q23 = make_float2(__fdiv_rn(x[4 * k + 2], s), __fdiv_rn(x[4 * k + 3], s));
@@ -292,6 +295,374 @@ __global__ void __launch_bounds__(kPrepThreads, D <= 128 ? 2 : 1) fp8_prepare_ke
   }
 }
 
+// ---------------------------------------------------------------------------
+// d = 128 with per-block scales: the streaming pre-pass.
+//
+// A persistent grid of two 512-thread CTAs per SM walks the (row block, head)
+// units in contiguous ranges, head fastest, so consecutive units read the same
+// rotary table rows.  A unit is three steps, Q, K and V of its 128 rows, each
+// with its own 32 KiB stage: while a CTA works on one step, each lane already
+// has its row of the next two steps in flight (16-byte asynchronous copies,
+// zero-filled past N, into the lane's own slots of the stage); a step's stage
+// is refilled with the same tensor of the next unit as soon as the step has
+// read it.  The three steps are unrolled, so the code has no branch on the
+// tensor.
+//
+// Row layout over the 4 lanes of its group: lane g holds the four 8-element
+// runs v*32 + g*8 + j (register index e = 8 v + j), so the group's global
+// accesses are 64 contiguous bytes.  The Hadamard butterflies of element bits
+// 0, 1, 2 (j) and 5, 6 (v) run in registers; a transpose through the warp's
+// slots of the step's stage (two halves of 16 values, XOR-swizzled so that
+// neither side has bank conflicts) then gives lane g the contiguous elements
+// 32 g .. 32 g + 31 (register index = element - 32 g), whose bits 3 and 4 take
+// the last two stages in registers.
+//
+// With the rotation, 1 / sqrt(d) is folded into the quantisation: the block
+// maximum of the unscaled values times 1 / sqrt(d) (rounding is monotone, so
+// this is the maximum of the scaled values, and s is the same float), then
+// code = RNE_satfinite(x RN(1 / (sqrt(d) s))): one product per value, within a
+// float32 rounding of x / (sqrt(d) s).  Without the rotation the codes keep the
+// FMA-corrected quotient, bit-exact against the float32 division.
+constexpr int kStreamD = 128;
+constexpr int kStreamStageBytes = kQuantRows * kStreamD * 2;  // 32 KiB: one tensor of a unit
+constexpr int kStreamSlotStride = kPrepThreads * 16;          // bytes between a lane's 4 slots
+constexpr int kStreamSmemBytes = 3 * kStreamStageBytes;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 r;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(addr)
+               : "memory");
+  return r;
+}
+
+// q = RN(a / b) from y = RN(1 / b) (FMA correction, as div_by_scale2).
+__device__ __forceinline__ float div_corrected(float a, float b, float y) {
+  const float q0 = a * y;
+  const float r = fmaf(-q0, b, a);
+  return fmaf(r, y, q0);
+}
+
+// Sign bit (bit 31) from bit 7 of byte `B` of w.
+template <int B>
+__device__ __forceinline__ uint32_t sign_of_byte(uint32_t w) {
+  return __byte_perm(w, 0u, 0x0444u | B << 12) & 0x80000000u;
+}
+
+// Unit cursor: row block and head (h = bh mod H), head fastest.
+struct PrepUnit {
+  int bh, h, blk;
+};
+__device__ __forceinline__ void next_unit(PrepUnit& u, int BH, int H) {
+  if (++u.h == H) u.h = 0;
+  if (++u.bh == BH) {
+    u.bh = 0;
+    ++u.blk;
+  }
+}
+
+template <bool BF16IN, bool ROPE>
+__global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(const PrepParams p, int n_units) {
+  constexpr int D = kStreamD, VPL = D / 4;
+  constexpr float kInvSqrtD = 0.08838834764831845f;
+  extern __shared__ __align__(128) uint8_t stream_smem[];
+  __shared__ unsigned int blk_amax[3];  // block maximum (float bits) of the Q, K and V steps
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane & 3, rw = lane >> 2;
+  const int rib = warp * 8 + rw;  // row in the 128-row block
+  const uint32_t sbase = smem_u32(stream_smem);
+  const int begin = static_cast<int>(static_cast<long long>(n_units) * blockIdx.x / gridDim.x);
+  const int end = static_cast<int>(static_cast<long long>(n_units) * (blockIdx.x + 1) / gridDim.x);
+  const bool rotate = p.signs != nullptr;
+  if (tid < 3) blk_amax[tid] = 0u;
+  __syncthreads();
+
+  // Row of this lane in a unit, as an index into the [B*H*N] rows (below 2^31:
+  // the host takes the generic kernel otherwise); rows past N copy nothing.
+  auto lane_row = [&](const PrepUnit& u, uint32_t& bytes) -> int {
+    const int row = u.blk * kQuantRows + rib;
+    bytes = row < p.N ? 16u : 0u;
+    return u.bh * p.N + (row < p.N ? row : 0);
+  };
+  // Copies of tensor T's rows of a unit into stage T (one commit group, empty
+  // past the CTA's range, so that every step waits for the same group count).
+  auto issue = [&](auto tc, bool live, int ridx, uint32_t bytes) {
+    constexpr int T = decltype(tc)::value;
+    if (live) {
+      const uint8_t* src = static_cast<const uint8_t*>(p.src[T]) + static_cast<size_t>(ridx) * (D * 2) + g * 16;
+      const uint32_t dst = sbase + T * kStreamStageBytes + tid * 16;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) cp_async16(dst + v * kStreamSlotStride, src + v * 64, bytes);
+    }
+    cp_async_commit();
+  };
+
+  PrepUnit cur;
+  cur.blk = begin / p.BH;
+  cur.bh = begin - cur.blk * p.BH;
+  cur.h = cur.bh % p.H;
+  {
+    uint32_t bytes;
+    const int ridx = lane_row(cur, bytes);
+    const bool live = begin < end;
+    issue(std::integral_constant<int, 0>(), live, ridx, bytes);
+    issue(std::integral_constant<int, 1>(), live, ridx, bytes);
+  }
+
+  for (int u = begin; u < end; ++u) {
+    const int row = cur.blk * kQuantRows + rib;
+    uint32_t cbytes;
+    const int ridx = lane_row(cur, cbytes);  // stores use it only for rows below N
+    const bool have = cbytes != 0u;
+    const int h = cur.h;
+    const int sidx = cur.bh * p.nblk + cur.blk;
+    next_unit(cur, p.BH, p.H);
+    uint32_t nbytes;
+    const int nridx = lane_row(cur, nbytes);
+    const bool nlive = u + 1 < end;
+
+    auto step = [&](auto tc) {
+      constexpr int T = decltype(tc)::value;
+      constexpr bool QK = T < 2;
+      const bool fwht = QK && rotate;  // uniform over the grid
+      // Refill the stage the previous step read: V of this unit before Q, then
+      // Q and K of the next unit; this step's copies are two groups back.
+      if constexpr (T == 0) issue(std::integral_constant<int, 2>(), true, ridx, cbytes);
+      else issue(std::integral_constant<int, T - 1>(), nlive, nridx, nbytes);
+      uint2 sw[4];
+      if (fwht) {
+        const int8_t* sg = p.signs + h * D + g * 8;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) sw[v] = *reinterpret_cast<const uint2*>(sg + v * 32);
+      }
+      cp_async_wait<2>();  // this step's group; the next two steps' stay in flight
+      const uint32_t st = sbase + T * kStreamStageBytes;
+      float x[VPL];
+      {
+        uint4 raw[4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) raw[v] = ld_shared_v4(st + v * kStreamSlotStride + tid * 16);
+        if (fwht) {
+          // Signs (+1 = 0x01, -1 = 0xff) onto the 16-bit words: bit 7 of each
+          // sign byte becomes the sign bit of its value (commutes with the
+          // widening and, through the sign of each sine, with the rotary step).
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            raw[v].x ^= __byte_perm(sw[v].x, 0u, 0x1404u) & 0x80008000u;
+            raw[v].y ^= __byte_perm(sw[v].x, 0u, 0x3424u) & 0x80008000u;
+            raw[v].z ^= __byte_perm(sw[v].y, 0u, 0x1404u) & 0x80008000u;
+            raw[v].w ^= __byte_perm(sw[v].y, 0u, 0x3424u) & 0x80008000u;
+          }
+        }
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint32_t w4[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float2 f;
+            if constexpr (BF16IN) f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[q]));
+            else f = __half22float2(*reinterpret_cast<const __half2*>(&w4[q]));
+            x[8 * v + 2 * q] = f.x;
+            x[8 * v + 2 * q + 1] = f.y;
+          }
+        }
+      }
+      if constexpr (QK && ROPE) {
+        if (have) {
+          // With the signs already on the inputs, pair (a, b) with signs (sa, sb)
+          // takes the rotation with sin * sa * sb, which gives sa (a c - b s) and
+          // sb (a s + b c), bit for bit (rounding is odd-symmetric).
+          const float* cr = p.rcos + static_cast<size_t>(row) * (D / 2);
+          const float* sr = p.rsin + static_cast<size_t>(row) * (D / 2);
+          if (p.rope_interleaved) {
+            // Pairs (2i, 2i+1): elements j, j+1 of run v, i = 16 v + 4 g + j / 2.
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const float4 c4 = *reinterpret_cast<const float4*>(cr + 16 * v + 4 * g);
+              float4 s4 = *reinterpret_cast<const float4*>(sr + 16 * v + 4 * g);
+              if (fwht) {
+                const uint32_t px = sw[v].x ^ (sw[v].x >> 8), py = sw[v].y ^ (sw[v].y >> 8);
+                s4.x = __uint_as_float(__float_as_uint(s4.x) ^ sign_of_byte<0>(px));
+                s4.y = __uint_as_float(__float_as_uint(s4.y) ^ sign_of_byte<2>(px));
+                s4.z = __uint_as_float(__float_as_uint(s4.z) ^ sign_of_byte<0>(py));
+                s4.w = __uint_as_float(__float_as_uint(s4.w) ^ sign_of_byte<2>(py));
+              }
+              const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, ss[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int e = 8 * v + 2 * q;
+                const float a = x[e], b = x[e + 1];
+                x[e] = fmaf(a, cc[q], -(b * ss[q]));
+                x[e + 1] = fmaf(a, ss[q], b * cc[q]);
+              }
+            }
+          } else {
+            // Pairs (i, i + d/2): element j of run v and of run v + 2, i = 32 v + 8 g + j.
+#pragma unroll
+            for (int v = 0; v < 2; ++v) {
+              uint2 pr = make_uint2(0u, 0u);
+              if (fwht) pr = make_uint2(sw[v].x ^ sw[v + 2].x, sw[v].y ^ sw[v + 2].y);
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const float4 c4 = *reinterpret_cast<const float4*>(cr + 32 * v + 8 * g + 4 * hh);
+                const float4 s4 = *reinterpret_cast<const float4*>(sr + 32 * v + 8 * g + 4 * hh);
+                const uint32_t pw = hh ? pr.y : pr.x;
+                const uint32_t m[4] = {sign_of_byte<0>(pw), sign_of_byte<1>(pw), sign_of_byte<2>(pw),
+                                       sign_of_byte<3>(pw)};
+                const float sv[4] = {s4.x, s4.y, s4.z, s4.w}, cv[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+                for (int q = 0; q < 4; q += 2) {
+                  const int e = 8 * v + 4 * hh + q;
+                  const float2 sp = make_float2(__uint_as_float(__float_as_uint(sv[q]) ^ m[q]),
+                                                __uint_as_float(__float_as_uint(sv[q + 1]) ^ m[q + 1]));
+                  const float2 sn = make_float2(-sp.x, -sp.y);
+                  const float2 a = pair(x, e), b = pair(x, e + 16);
+                  const float2 c2 = make_float2(cv[q], cv[q + 1]);
+                  put(x, e, ffma2(b, sn, fmul2(a, c2)));
+                  put(x, e + 16, ffma2(a, sp, fmul2(b, c2)));
+                }
+              }
+            }
+          }
+        }
+      }
+
+      if (fwht) {
+        // Element bits 0 (scalar: the two halves of a register pair), 1, 2, 5, 6.
+#pragma unroll
+        for (int e = 0; e < VPL; e += 2) {
+          const float a = x[e], b = x[e + 1];
+          x[e] = a + b;
+          x[e + 1] = a - b;
+        }
+#pragma unroll
+        for (int m = 2; m < VPL; m <<= 1)
+#pragma unroll
+          for (int e = 0; e < VPL; e += 2)
+            if ((e & m) == 0) {
+              const float2 a = pair(x, e), b = pair(x, e + m);
+              put(x, e, fadd2(a, b));
+              put(x, e + m, fsub2(a, b));
+            }
+        // Transpose within the row's group: unit (run 4 a + b, half hh) of row rw
+        // sits in segment a at byte rw * 64 + ((b ^ a) * 16) of the warp's
+        // 512-byte share; the writer is lane b (a = its run v), the reader lane a.
+        __syncwarp();  // every lane has read its own slots
+        const uint32_t wbase = st + warp * 512 + rw * 64;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int e = 8 * v + 4 * hh;
+            st_shared_v4(wbase + v * kStreamSlotStride + ((g ^ v) << 4), __float_as_uint(x[e]),
+                         __float_as_uint(x[e + 1]), __float_as_uint(x[e + 2]), __float_as_uint(x[e + 3]));
+          }
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 r = ld_shared_v4(wbase + g * kStreamSlotStride + ((k ^ g) << 4));
+            const int e = 8 * k + 4 * hh;
+            x[e] = __uint_as_float(r.x);
+            x[e + 1] = __uint_as_float(r.y);
+            x[e + 2] = __uint_as_float(r.z);
+            x[e + 3] = __uint_as_float(r.w);
+          }
+          __syncwarp();
+        }
+        // Element bits 3 and 4 (register index bits 3 and 4 of 32 g + e).
+#pragma unroll
+        for (int m = 8; m < VPL; m <<= 1)
+#pragma unroll
+          for (int e = 0; e < VPL; e += 2)
+            if ((e & m) == 0) {
+              const float2 a = pair(x, e), b = pair(x, e + m);
+              put(x, e, fadd2(a, b));
+              put(x, e + m, fsub2(a, b));
+            }
+      }
+
+      // Block maximum of |x|: max and min chains (no per-value absolute
+      // value), the warp's maximum on the float bits (non-negative values order
+      // as unsigned integers), one shared atomic per warp, one barrier.
+      float mx = fmaxf(x[0], x[1]), mn = fminf(x[0], x[1]);
+#pragma unroll
+      for (int e = 2; e < VPL; e += 2) {
+        mx = max3(mx, x[e], x[e + 1]);
+        mn = min3(mn, x[e], x[e + 1]);
+      }
+      const unsigned int wmax =
+          __reduce_max_sync(0xffffffffu, __float_as_uint(fmaxf(mx, -mn)) & 0x7fffffffu);
+      if (lane == 0) atomicMax(&blk_amax[T], wmax);
+      if (tid == 0) blk_amax[(T + 1) % 3] = 0u;  // last read two steps ago, before the previous barrier
+      __syncthreads();
+      float amax = __uint_as_float(blk_amax[T]);
+      if (fwht) amax *= kInvSqrtD;
+      // Ordinary maxima take s by the FMA-corrected quotient and the codes by
+      // products; the rest (uniform over the CTA) divide.
+      const bool fast = __all_sync(0xffffffffu, amax >= 0x1p-90f && amax <= 0x1p+100f);
+      const float s = fast ? div_corrected(amax, kE4M3Max, 1.0f / kE4M3Max) : (amax > 0.f ? amax / kE4M3Max : 1.f);
+      if (tid == 0) p.scale[T][sidx] = s;
+      uint32_t pk[8];
+      if (fast) {
+        const float y = __frcp_rn(s);
+        if (fwht) {
+          const float yds = div_corrected(kInvSqrtD, s, y);
+          const float2 y2 = make_float2(yds, yds);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t lo = __nv_cvt_float2_to_fp8x2(fmul2(pair(x, 4 * q), y2), __NV_SATFINITE, __NV_E4M3);
+            const uint32_t hi = __nv_cvt_float2_to_fp8x2(fmul2(pair(x, 4 * q + 2), y2), __NV_SATFINITE, __NV_E4M3);
+            pk[q] = lo | (hi << 16);
+          }
+        } else {
+          const float2 s2 = make_float2(s, s), ny2 = make_float2(-y, -y), y2 = make_float2(y, y);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t lo =
+                __nv_cvt_float2_to_fp8x2(div_by_scale2(pair(x, 4 * q), s2, ny2, y2), __NV_SATFINITE, __NV_E4M3);
+            const uint32_t hi = __nv_cvt_float2_to_fp8x2(div_by_scale2(pair(x, 4 * q + 2), s2, ny2, y2),
+                                                         __NV_SATFINITE, __NV_E4M3);
+            pk[q] = lo | (hi << 16);
+          }
+        }
+      } else {
+        const float c = fwht ? kInvSqrtD : 1.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float2 q01 = make_float2(__fdiv_rn(x[4 * q] * c, s), __fdiv_rn(x[4 * q + 1] * c, s));
+          const float2 q23 = make_float2(__fdiv_rn(x[4 * q + 2] * c, s), __fdiv_rn(x[4 * q + 3] * c, s));
+          const uint32_t lo = __nv_cvt_float2_to_fp8x2(q01, __NV_SATFINITE, __NV_E4M3);
+          const uint32_t hi = __nv_cvt_float2_to_fp8x2(q23, __NV_SATFINITE, __NV_E4M3);
+          pk[q] = lo | (hi << 16);
+        }
+      }
+      if (have) {
+        uint8_t* dst = p.dst[T] + static_cast<size_t>(ridx) * D;
+        if (fwht) {
+          uint4* out = reinterpret_cast<uint4*>(dst + 32 * g);
+          out[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          out[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        } else {
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            *reinterpret_cast<uint2*>(dst + 32 * v + 8 * g) = make_uint2(pk[2 * v], pk[2 * v + 1]);
+        }
+      }
+    };
+    step(std::integral_constant<int, 0>());
+    step(std::integral_constant<int, 1>());
+    step(std::integral_constant<int, 2>());
+  }
+}
+
 // Per-tensor mode: the scale slot held the tensor amax (as bits); turn it into s.
 __global__ void fp8_finalize_scale_kernel(float* q_scale, float* k_scale, float* v_scale) {
   float* sc[3] = {q_scale, k_scale, v_scale};
@@ -301,9 +672,34 @@ __global__ void fp8_finalize_scale_kernel(float* q_scale, float* k_scale, float*
   }
 }
 
+// d = 128, per-block scales: the streaming pre-pass, two CTAs per SM.
+template <bool BF16IN, bool ROPE>
+attn_status run_prepare_stream(const PrepParams& prm, cudaStream_t s) {
+  static int configured_for[64] = {0};  // per device: dynamic shared memory attribute set
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return attn_internal::cuda_status(e);
+  if (dev >= 64 || !configured_for[dev]) {
+    e = cudaFuncSetAttribute(fp8_prepare_stream_kernel<BF16IN, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kStreamSmemBytes);
+    if (e != cudaSuccess) return attn_internal::cuda_status(e);
+    if (dev < 64) configured_for[dev] = 1;
+  }
+  const int sms = attn_internal::sm_count();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  const int n_units = prm.BH * prm.nblk;  // (row block, head) units, three steps each
+  const int grid = n_units < 2 * sms ? n_units : 2 * sms;
+  fp8_prepare_stream_kernel<BF16IN, ROPE><<<grid, kPrepThreads, kStreamSmemBytes, s>>>(prm, n_units);
+  return attn_internal::cuda_status(cudaGetLastError());
+}
+
 template <int D, bool BF16IN>
 attn_status run_prepare_d(const PrepParams& prm, int per_tensor, cudaStream_t s) {
   const dim3 grid(static_cast<unsigned>(prm.BH) * prm.nblk, 3);
+  if constexpr (D == kStreamD) {
+    if (!per_tensor && static_cast<long long>(prm.BH) * prm.N < 0x7fffffffll)
+      return prm.rcos != nullptr ? run_prepare_stream<BF16IN, true>(prm, s) : run_prepare_stream<BF16IN, false>(prm, s);
+  }
   if (!per_tensor) {
     fp8_prepare_kernel<D, BF16IN, PREP_BLOCK><<<grid, kPrepThreads, 0, s>>>(prm);
     return attn_internal::cuda_status(cudaGetLastError());

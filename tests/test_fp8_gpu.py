@@ -49,8 +49,7 @@ PREP_D = [64, 128, 256]
 def test_prepare_without_rotation_is_bit_exact(dtype, d):
     """No rotation: both sides divide the same float32 value by the same scale
     and round to nearest even, so every code and every scale is identical.
-    Several (block, tensor, head) items per CTA of the persistent pre-pass,
-    and a ragged last block."""
+    A ragged last block."""
     q, k, v = synth.outlier_inputs(2, 3, 300, d, dtype, seed=1)
     out = attn.fp8_prepare(q.cuda(), k.cuda(), v.cuda(), signs=None)
     torch.cuda.synchronize()
@@ -58,6 +57,30 @@ def test_prepare_without_rotation_is_bit_exact(dtype, d):
         codes, scales = oracle.block_quantize(x)
         np.testing.assert_array_equal(_np(c), codes)
         np.testing.assert_array_equal(_np(s), scales)
+
+
+@pytest.mark.parametrize("d", PREP_D)
+@pytest.mark.parametrize("per_tensor", [False, True])
+def test_prepare_keeps_the_sign_of_zero(d, per_tensor):
+    """Exact zeros of either sign (and the smallest subnormals) in unrotated
+    tensors: code = RNE(x / s) keeps the sign, so -0 gives 0x80 and +0 gives
+    0x00, bit-exact against the oracle."""
+    q, k, v = synth.outlier_inputs(2, 3, 300, d, "fp16", seed=14)
+    g = torch.Generator().manual_seed(14)
+    for t in (q, k, v):
+        flat = t.view(-1)
+        idx = torch.randperm(flat.numel(), generator=g)[:4000]
+        flat[idx[:1000]] = -0.0
+        flat[idx[1000:2000]] = 0.0
+        flat[idx[2000:3000]] = -2.0 ** -24
+        flat[idx[3000:]] = 2.0 ** -24
+    out = attn.fp8_prepare(q.cuda(), k.cuda(), v.cuda(), signs=None, per_tensor=per_tensor)
+    torch.cuda.synchronize()
+    for x, c, s in zip((q, k, v), out[:3], out[3:]):
+        codes, scales = oracle.block_quantize(x, per_tensor=per_tensor)
+        assert np.sum(codes == 0x80) >= 1000
+        np.testing.assert_array_equal(_np(s), scales)
+        np.testing.assert_array_equal(_np(c), codes)
 
 
 @pytest.mark.parametrize("d", PREP_D)
@@ -261,10 +284,10 @@ def test_fp8_empty_and_bad_arguments():
 
 @pytest.mark.parametrize("d", PREP_D)
 def test_prepare_many_items_per_cta(d):
-    """A problem with many more (block, tensor, head) items than CTAs, so every
-    CTA of the persistent pre-pass walks a long range of items through its
-    ring of copies (and crosses block boundaries): codes and scales bit-exact
-    against the oracle without rotation."""
+    """A problem with many more (block, tensor, head) items than CTAs: at
+    d = 128 every CTA of the streaming pre-pass walks a long range of items
+    through its ring of copies (crossing block boundaries); codes and scales
+    bit-exact against the oracle without rotation."""
     B, H, N = 4, 8, 2048 + 77
     q, k, v = synth.outlier_inputs(B, H, N, d, "bf16", seed=12)
     out = attn.fp8_prepare(q.cuda(), k.cuda(), v.cuda(), signs=None)
@@ -276,6 +299,31 @@ def test_prepare_many_items_per_cta(d):
     assert attn.device_status() == attn.ATTN_OK
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("rope", [None, "half", "interleaved"])
+def test_prepare_rotation_many_items_per_cta(rope, dtype):
+    """d = 128 streams (block, tensor, head) items through a ring of copies on
+    a grid of two CTAs per SM: with many items per CTA, Q and K with the
+    rotation (and the rotary embedding) against the oracle within one E4M3
+    step, V bit-exact, and a ragged last block."""
+    B, H, N, d = 4, 8, 2048 + 77, 128
+    q, k, v = synth.outlier_inputs(B, H, N, d, dtype, seed=13)
+    signs = synth.hadamard_signs(H, d, seed=13)
+    tables = synth.rotary_tables(N, d, offset=3) if rope else None
+    out = attn.fp8_prepare(q.cuda(), k.cuda(), v.cuda(), signs=signs.cuda(),
+                           rope=None if tables is None else tuple(t.cuda() for t in tables),
+                           rope_interleaved=rope == "interleaved")
+    torch.cuda.synchronize()
+    for i, x in enumerate((q, k)):
+        ref = x if tables is None else oracle.rotary(x, *tables, rope == "interleaved")
+        codes, scales = oracle.block_quantize(oracle.hadamard_rotate(ref, signs))
+        _assert_codes_within_one_step(_np(out[i]), _np(out[3 + i]), codes, scales)
+    codes, scales = oracle.block_quantize(v)
+    np.testing.assert_array_equal(_np(out[2]), codes)
+    np.testing.assert_array_equal(_np(out[5]), scales)
+    assert attn.device_status() == attn.ATTN_OK
+
+
 @pytest.mark.parametrize("d", PREP_D)
 @pytest.mark.parametrize("interleaved", [False, True])
 @pytest.mark.parametrize("rotate", [False, True])
@@ -284,8 +332,7 @@ def test_prepare_with_rotary_matches_oracle(interleaved, rotate, d):
     oracle's rotary -> rotation -> block quantisation (float32 on the device,
     float64 in the oracle: scales to float32 rounding, dequantised values within
     one E4M3 step, few codes different); V untouched, bit-exact.  N = 385 leaves
-    a ragged last block (rows past N skip the table loads).  d <= 128 stages
-    the table rows in shared memory, d = 256 reads them from global memory."""
+    a ragged last block (rows past N skip the table loads)."""
     B, H, N = 2, 3, 385
     q, k, v = synth.outlier_inputs(B, H, N, d, "bf16", seed=7)
     signs = synth.hadamard_signs(H, d, seed=7) if rotate else None
