@@ -327,6 +327,7 @@ constexpr int kStreamD = 128;
 constexpr int kStreamStageBytes = kQuantRows * kStreamD * 2;  // 32 KiB: one tensor of a unit
 constexpr int kStreamSlotStride = kPrepThreads * 16;          // bytes between a lane's 4 slots
 constexpr int kStreamSmemBytes = 3 * kStreamStageBytes;
+constexpr int kStreamMaskHeads = 32;  // sign masks of up to this many heads sit in shared memory
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
@@ -343,6 +344,33 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                : "r"(addr)
                : "memory");
   return r;
+}
+
+// Per-halfword unsigned maximum of two packed pairs.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// (x0 + x1, x0 - x1) of the 16-bit pair w (x0 in the low half), each with one
+// rounding, as the float32 sum and difference of the widened values: the
+// mixed-precision add and subtract take x0 in its 16-bit form.
+template <bool BF16IN>
+__device__ __forceinline__ float2 widen_butterfly(uint32_t w) {
+  float s, d;
+  if constexpr (BF16IN) {
+    const float x1 = __uint_as_float(w & 0xffff0000u);
+    asm("{.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tadd.rn.f32.bf16 %0, l, %3;\n\tsub.rn.f32.bf16 %1, l, %3;}"
+        : "=f"(s), "=f"(d)
+        : "r"(w), "f"(x1));
+  } else {
+    asm("{.reg .b16 l, h;\n\t.reg .f32 x1;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 x1, h;\n\t"
+        "add.rn.f32.f16 %0, l, x1;\n\tsub.rn.f32.f16 %1, l, x1;}"
+        : "=f"(s), "=f"(d)
+        : "r"(w));
+  }
+  return make_float2(s, d);
 }
 
 // q = RN(a / b) from y = RN(1 / b) (FMA correction, as div_by_scale2).
@@ -375,14 +403,26 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
   constexpr int D = kStreamD, VPL = D / 4;
   constexpr float kInvSqrtD = 0.08838834764831845f;
   extern __shared__ __align__(128) uint8_t stream_smem[];
-  __shared__ unsigned int blk_amax[3];  // block maximum (float bits) of the Q, K and V steps
+  // Block maxima (float bits) of Q, K and V, double-buffered by unit parity.
+  __shared__ unsigned int blk_amax[2][3];
+  // Sign masks of the heads (H <= 32): word (h, g, v, q) holds the signs of
+  // elements 32 v + 8 g + 2 q and + 1 at bits 15 and 31, as the 16-bit pair.
+  __shared__ __align__(16) uint32_t mask_tab[kStreamMaskHeads * 64];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane & 3, rw = lane >> 2;
   const int rib = warp * 8 + rw;  // row in the 128-row block
   const uint32_t sbase = smem_u32(stream_smem);
   const int begin = static_cast<int>(static_cast<long long>(n_units) * blockIdx.x / gridDim.x);
   const int end = static_cast<int>(static_cast<long long>(n_units) * (blockIdx.x + 1) / gridDim.x);
   const bool rotate = p.signs != nullptr;
-  if (tid < 3) blk_amax[tid] = 0u;
+  const bool mask_smem = !ROPE && p.H <= kStreamMaskHeads;
+  if (tid < 6) (&blk_amax[0][0])[tid] = 0u;
+  if (rotate && mask_smem)
+    for (int i = tid; i < p.H * 64; i += kPrepThreads) {
+      const int e0 = ((i >> 2) & 3) * 32 + ((i >> 4) & 3) * 8 + (i & 3) * 2;
+      const int8_t* sg = p.signs + (i >> 6) * D + e0;
+      mask_tab[i] = (static_cast<uint32_t>(static_cast<uint8_t>(sg[0]) & 0x80u) << 8) |
+                    (static_cast<uint32_t>(static_cast<uint8_t>(sg[1]) & 0x80u) << 24);
+    }
   __syncthreads();
 
   // Row of this lane in a unit, as an index into the [B*H*N] rows (below 2^31:
@@ -418,16 +458,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
   }
 
   for (int u = begin; u < end; ++u) {
-    const int row = cur.blk * kQuantRows + rib;
-    uint32_t cbytes;
-    const int ridx = lane_row(cur, cbytes);  // stores use it only for rows below N
-    const bool have = cbytes != 0u;
-    const int h = cur.h;
-    const int sidx = cur.bh * p.nblk + cur.blk;
-    next_unit(cur, p.BH, p.H);
-    uint32_t nbytes;
-    const int nridx = lane_row(cur, nbytes);
-    const bool nlive = u + 1 < end;
+    const int par = u & 1;
+    // Per-lane values are recomputed where they are used (registers are the
+    // limit at two CTAs per SM).
 
     auto step = [&](auto tc) {
       constexpr int T = decltype(tc)::value;
@@ -435,10 +468,23 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
       const bool fwht = QK && rotate;  // uniform over the grid
       // Refill the stage the previous step read: V of this unit before Q, then
       // Q and K of the next unit; this step's copies are two groups back.
-      if constexpr (T == 0) issue(std::integral_constant<int, 2>(), true, ridx, cbytes);
-      else issue(std::integral_constant<int, T - 1>(), nlive, nridx, nbytes);
-      uint2 sw[4];
-      if (fwht) {
+      if constexpr (T == 0) {
+        uint32_t bytes;
+        const int r = lane_row(cur, bytes);
+        issue(std::integral_constant<int, 2>(), true, r, bytes);
+      } else {
+        PrepUnit nx = cur;
+        next_unit(nx, p.BH, p.H);
+        uint32_t bytes;
+        const int r = lane_row(nx, bytes);
+        issue(std::integral_constant<int, T - 1>(), u + 1 < end, r, bytes);
+      }
+      const int h = cur.h;
+      // Without the rotary step the widening and the first butterfly (element
+      // bit 0) are one step: x0 + x1 and x0 - x1 straight from the 16-bit pair.
+      const bool fused = fwht && !ROPE;
+      uint2 sw[4];  // sign bytes, where the masks are not in shared memory
+      if (fwht && !mask_smem) {
         const int8_t* sg = p.signs + h * D + g * 8;
 #pragma unroll
         for (int v = 0; v < 4; ++v) sw[v] = *reinterpret_cast<const uint2*>(sg + v * 32);
@@ -456,10 +502,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
           // widening and, through the sign of each sine, with the rotary step).
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            raw[v].x ^= __byte_perm(sw[v].x, 0u, 0x1404u) & 0x80008000u;
-            raw[v].y ^= __byte_perm(sw[v].x, 0u, 0x3424u) & 0x80008000u;
-            raw[v].z ^= __byte_perm(sw[v].y, 0u, 0x1404u) & 0x80008000u;
-            raw[v].w ^= __byte_perm(sw[v].y, 0u, 0x3424u) & 0x80008000u;
+            if (mask_smem) {
+              const uint4 m = *reinterpret_cast<const uint4*>(&mask_tab[(h * 4 + g) * 16 + v * 4]);
+              raw[v].x ^= m.x;
+              raw[v].y ^= m.y;
+              raw[v].z ^= m.z;
+              raw[v].w ^= m.w;
+            } else {
+              raw[v].x ^= __byte_perm(sw[v].x, 0u, 0x1404u) & 0x80008000u;
+              raw[v].y ^= __byte_perm(sw[v].x, 0u, 0x3424u) & 0x80008000u;
+              raw[v].z ^= __byte_perm(sw[v].y, 0u, 0x1404u) & 0x80008000u;
+              raw[v].w ^= __byte_perm(sw[v].y, 0u, 0x3424u) & 0x80008000u;
+            }
           }
         }
 #pragma unroll
@@ -468,7 +522,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             float2 f;
-            if constexpr (BF16IN) f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[q]));
+            if (fused) f = widen_butterfly<BF16IN>(w4[q]);
+            else if constexpr (BF16IN) f = make_float2(__uint_as_float(w4[q] << 16), __uint_as_float(w4[q] & 0xffff0000u));
             else f = __half22float2(*reinterpret_cast<const __half2*>(&w4[q]));
             x[8 * v + 2 * q] = f.x;
             x[8 * v + 2 * q + 1] = f.y;
@@ -476,7 +531,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
         }
       }
       if constexpr (QK && ROPE) {
-        if (have) {
+        const int row = cur.blk * kQuantRows + rib;
+        if (row < p.N) {
           // With the signs already on the inputs, pair (a, b) with signs (sa, sb)
           // takes the rotation with sin * sa * sb, which gives sa (a c - b s) and
           // sb (a s + b c), bit for bit (rounding is odd-symmetric).
@@ -536,12 +592,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
       }
 
       if (fwht) {
-        // Element bits 0 (scalar: the two halves of a register pair), 1, 2, 5, 6.
+        // Element bits 0 (scalar: the two halves of a register pair; done with
+        // the widening when fused), 1, 2, 5, 6.
+        if (!fused) {
 #pragma unroll
-        for (int e = 0; e < VPL; e += 2) {
-          const float a = x[e], b = x[e + 1];
-          x[e] = a + b;
-          x[e + 1] = a - b;
+          for (int e = 0; e < VPL; e += 2) {
+            const float a = x[e], b = x[e + 1];
+            x[e] = a + b;
+            x[e + 1] = a - b;
+          }
         }
 #pragma unroll
         for (int m = 2; m < VPL; m <<= 1)
@@ -589,32 +648,68 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
             }
       }
 
-      // Block maximum of |x|: max and min chains (no per-value absolute
-      // value), the warp's maximum on the float bits (non-negative values order
-      // as unsigned integers), one shared atomic per warp, one barrier.
-      float mx = fmaxf(x[0], x[1]), mn = fminf(x[0], x[1]);
+      // Block maximum of |x|.  Q and K: max and min over four independent
+      // chains (no per-value absolute value), the warp's maximum on the float
+      // bits (non-negative values order as unsigned integers), one shared
+      // atomic per warp and one barrier.  V has no barrier of its own: the K
+      // step takes V's maximum from its 16-bit words (|x| orders as the bits
+      // without the sign, read as unsigned) and its barrier publishes both.
+      if constexpr (QK) {
+        float mx[4], mn[4];
 #pragma unroll
-      for (int e = 2; e < VPL; e += 2) {
-        mx = max3(mx, x[e], x[e + 1]);
-        mn = min3(mn, x[e], x[e + 1]);
+        for (int c = 0; c < 4; ++c) {
+          mx[c] = fmaxf(x[8 * c], x[8 * c + 1]);
+          mn[c] = fminf(x[8 * c], x[8 * c + 1]);
+#pragma unroll
+          for (int e = 8 * c + 2; e < 8 * c + 8; e += 2) {
+            mx[c] = max3(mx[c], x[e], x[e + 1]);
+            mn[c] = min3(mn[c], x[e], x[e + 1]);
+          }
+        }
+        const float m = fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]);
+        const float n = fminf(min3(mn[0], mn[1], mn[2]), mn[3]);
+        const unsigned int wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(fmaxf(m, -n)) & 0x7fffffffu);
+        if (lane == 0) atomicMax(&blk_amax[par][T], wmax);
+        if constexpr (T == 1) {
+          cp_async_wait<1>();  // V of this unit has arrived too
+          const uint32_t sv = sbase + 2 * kStreamStageBytes + tid * 16;
+          uint32_t vm = 0u;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint4 r = ld_shared_v4(sv + v * kStreamSlotStride);
+            vm = max_u16x2(vm, max_u16x2(max_u16x2(r.x & 0x7fff7fffu, r.y & 0x7fff7fffu),
+                                         max_u16x2(r.z & 0x7fff7fffu, r.w & 0x7fff7fffu)));
+          }
+          vm = max(vm & 0xffffu, vm >> 16);
+          float va;
+          if constexpr (BF16IN) va = __uint_as_float(vm << 16);
+          else va = __half2float(__ushort_as_half(static_cast<unsigned short>(vm)));
+          const unsigned int vwmax = __reduce_max_sync(0xffffffffu, __float_as_uint(va));
+          if (lane == 0) atomicMax(&blk_amax[par][2], vwmax);
+        }
+        __syncthreads();
+        // Unit u - 1 read its maxima before this barrier; unit u + 1 adds to them
+        // only after the K barrier, which these threads reach after the reset.
+        if (T == 0 && tid < 3) blk_amax[par ^ 1][tid] = 0u;
       }
-      const unsigned int wmax =
-          __reduce_max_sync(0xffffffffu, __float_as_uint(fmaxf(mx, -mn)) & 0x7fffffffu);
-      if (lane == 0) atomicMax(&blk_amax[T], wmax);
-      if (tid == 0) blk_amax[(T + 1) % 3] = 0u;  // last read two steps ago, before the previous barrier
-      __syncthreads();
-      float amax = __uint_as_float(blk_amax[T]);
+      float amax = __uint_as_float(blk_amax[par][T]);
+      const float amax_u = amax;  // with the rotation: the maximum before 1 / sqrt(d)
       if (fwht) amax *= kInvSqrtD;
       // Ordinary maxima take s by the FMA-corrected quotient and the codes by
       // products; the rest (uniform over the CTA) divide.
       const bool fast = __all_sync(0xffffffffu, amax >= 0x1p-90f && amax <= 0x1p+100f);
       const float s = fast ? div_corrected(amax, kE4M3Max, 1.0f / kE4M3Max) : (amax > 0.f ? amax / kE4M3Max : 1.f);
-      if (tid == 0) p.scale[T][sidx] = s;
+      if (tid == 0) p.scale[T][cur.bh * p.nblk + cur.blk] = s;
       uint32_t pk[8];
       if (fast) {
-        const float y = __frcp_rn(s);
         if (fwht) {
-          const float yds = div_corrected(kInvSqrtD, s, y);
+          // Rotated rows (float32 butterflies, compared within one E4M3 step):
+          // x / (sqrt(d) s) as x times 448 / amax_u, from the hardware
+          // reciprocal (within a few float32 roundings of the quotient), so the
+          // path from the barrier to the codes is one reciprocal and products.
+          float r;
+          asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(amax_u));
+          const float yds = r * kE4M3Max;
           const float2 y2 = make_float2(yds, yds);
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
@@ -623,6 +718,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
             pk[q] = lo | (hi << 16);
           }
         } else {
+          const float y = __frcp_rn(s);
           const float2 s2 = make_float2(s, s), ny2 = make_float2(-y, -y), y2 = make_float2(y, y);
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
@@ -644,8 +740,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
           pk[q] = lo | (hi << 16);
         }
       }
-      if (have) {
-        uint8_t* dst = p.dst[T] + static_cast<size_t>(ridx) * D;
+      const int row = cur.blk * kQuantRows + rib;
+      if (row < p.N) {
+        uint8_t* dst = p.dst[T] + (static_cast<size_t>(cur.bh) * p.N + row) * D;
         if (fwht) {
           uint4* out = reinterpret_cast<uint4*>(dst + 32 * g);
           out[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -660,6 +757,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
     step(std::integral_constant<int, 0>());
     step(std::integral_constant<int, 1>());
     step(std::integral_constant<int, 2>());
+    next_unit(cur, p.BH, p.H);
   }
 }
 
