@@ -386,6 +386,25 @@ __device__ __forceinline__ uint32_t sign_of_byte(uint32_t w) {
   return __byte_perm(w, 0u, 0x0444u | B << 12) & 0x80000000u;
 }
 
+// Lane indices of the thread, read through an empty volatile asm so that the
+// compiler re-derives them (and the addresses built from them) where they are
+// used instead of holding them in registers for the whole kernel.
+struct LaneIds {
+  int tid, warp, lane, g, rw, rib;  // rib: row in the 128-row block
+};
+__device__ __forceinline__ LaneIds lane_ids() {
+  int t = threadIdx.x;
+  asm volatile("" : "+r"(t));
+  LaneIds l;
+  l.tid = t;
+  l.warp = t >> 5;
+  l.lane = t & 31;
+  l.g = t & 3;
+  l.rw = (t & 31) >> 2;
+  l.rib = l.warp * 8 + l.rw;
+  return l;
+}
+
 // Unit cursor: row block and head (h = bh mod H), head fastest.
 struct PrepUnit {
   int bh, h, blk;
@@ -408,16 +427,17 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
   // Sign masks of the heads (H <= 32): word (h, g, v, q) holds the signs of
   // elements 32 v + 8 g + 2 q and + 1 at bits 15 and 31, as the 16-bit pair.
   __shared__ __align__(16) uint32_t mask_tab[kStreamMaskHeads * 64];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane & 3, rw = lane >> 2;
-  const int rib = warp * 8 + rw;  // row in the 128-row block
+  // Lane indices are re-read in every step (lane_ids), so that the per-lane
+  // addresses derived from them are not kept live across the whole loop.
+  const int tid0 = threadIdx.x;
   const uint32_t sbase = smem_u32(stream_smem);
   const int begin = static_cast<int>(static_cast<long long>(n_units) * blockIdx.x / gridDim.x);
   const int end = static_cast<int>(static_cast<long long>(n_units) * (blockIdx.x + 1) / gridDim.x);
   const bool rotate = p.signs != nullptr;
   const bool mask_smem = !ROPE && p.H <= kStreamMaskHeads;
-  if (tid < 6) (&blk_amax[0][0])[tid] = 0u;
+  if (tid0 < 6) (&blk_amax[0][0])[tid0] = 0u;
   if (rotate && mask_smem)
-    for (int i = tid; i < p.H * 64; i += kPrepThreads) {
+    for (int i = tid0; i < p.H * 64; i += kPrepThreads) {
       const int e0 = ((i >> 2) & 3) * 32 + ((i >> 4) & 3) * 8 + (i & 3) * 2;
       const int8_t* sg = p.signs + (i >> 6) * D + e0;
       mask_tab[i] = (static_cast<uint32_t>(static_cast<uint8_t>(sg[0]) & 0x80u) << 8) |
@@ -428,7 +448,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
   // Row of this lane in a unit, as an index into the [B*H*N] rows (below 2^31:
   // the host takes the generic kernel otherwise); rows past N copy nothing.
   auto lane_row = [&](const PrepUnit& u, uint32_t& bytes) -> int {
-    const int row = u.blk * kQuantRows + rib;
+    const int row = u.blk * kQuantRows + lane_ids().rib;
     bytes = row < p.N ? 16u : 0u;
     return u.bh * p.N + (row < p.N ? row : 0);
   };
@@ -437,8 +457,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
   auto issue = [&](auto tc, bool live, int ridx, uint32_t bytes) {
     constexpr int T = decltype(tc)::value;
     if (live) {
-      const uint8_t* src = static_cast<const uint8_t*>(p.src[T]) + static_cast<size_t>(ridx) * (D * 2) + g * 16;
-      const uint32_t dst = sbase + T * kStreamStageBytes + tid * 16;
+      const LaneIds L = lane_ids();
+      const uint8_t* src = static_cast<const uint8_t*>(p.src[T]) + static_cast<size_t>(ridx) * (D * 2) + L.g * 16;
+      const uint32_t dst = sbase + T * kStreamStageBytes + L.tid * 16;
 #pragma unroll
       for (int v = 0; v < 4; ++v) cp_async16(dst + v * kStreamSlotStride, src + v * 64, bytes);
     }
@@ -466,6 +487,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
       constexpr int T = decltype(tc)::value;
       constexpr bool QK = T < 2;
       const bool fwht = QK && rotate;  // uniform over the grid
+      const LaneIds L = lane_ids();
+      const int tid = L.tid, warp = L.warp, lane = L.lane, g = L.g, rw = L.rw, rib = L.rib;
       // Refill the stage the previous step read: V of this unit before Q, then
       // Q and K of the next unit; this step's copies are two groups back.
       if constexpr (T == 0) {
@@ -490,6 +513,25 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
         for (int v = 0; v < 4; ++v) sw[v] = *reinterpret_cast<const uint2*>(sg + v * 32);
       }
       cp_async_wait<2>();  // this step's group; the next two steps' stay in flight
+      if constexpr (T == 1) {
+        // V of this unit (its copies are one group behind K's): its block
+        // maximum goes out before K's registers fill up.
+        cp_async_wait<1>();
+        const uint32_t sv = sbase + 2 * kStreamStageBytes + tid * 16;
+        uint32_t vm = 0u;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint4 r = ld_shared_v4(sv + v * kStreamSlotStride);
+          vm = max_u16x2(vm, max_u16x2(max_u16x2(r.x & 0x7fff7fffu, r.y & 0x7fff7fffu),
+                                       max_u16x2(r.z & 0x7fff7fffu, r.w & 0x7fff7fffu)));
+        }
+        vm = max(vm & 0xffffu, vm >> 16);
+        float va;
+        if constexpr (BF16IN) va = __uint_as_float(vm << 16);
+        else va = __half2float(__ushort_as_half(static_cast<unsigned short>(vm)));
+        const unsigned int vwmax = __reduce_max_sync(0xffffffffu, __float_as_uint(va));
+        if (lane == 0) atomicMax(&blk_amax[par][2], vwmax);
+      }
       const uint32_t st = sbase + T * kStreamStageBytes;
       float x[VPL];
       {
@@ -670,23 +712,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
         const float n = fminf(min3(mn[0], mn[1], mn[2]), mn[3]);
         const unsigned int wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(fmaxf(m, -n)) & 0x7fffffffu);
         if (lane == 0) atomicMax(&blk_amax[par][T], wmax);
-        if constexpr (T == 1) {
-          cp_async_wait<1>();  // V of this unit has arrived too
-          const uint32_t sv = sbase + 2 * kStreamStageBytes + tid * 16;
-          uint32_t vm = 0u;
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const uint4 r = ld_shared_v4(sv + v * kStreamSlotStride);
-            vm = max_u16x2(vm, max_u16x2(max_u16x2(r.x & 0x7fff7fffu, r.y & 0x7fff7fffu),
-                                         max_u16x2(r.z & 0x7fff7fffu, r.w & 0x7fff7fffu)));
-          }
-          vm = max(vm & 0xffffu, vm >> 16);
-          float va;
-          if constexpr (BF16IN) va = __uint_as_float(vm << 16);
-          else va = __half2float(__ushort_as_half(static_cast<unsigned short>(vm)));
-          const unsigned int vwmax = __reduce_max_sync(0xffffffffu, __float_as_uint(va));
-          if (lane == 0) atomicMax(&blk_amax[par][2], vwmax);
-        }
         __syncthreads();
         // Unit u - 1 read its maxima before this barrier; unit u + 1 adds to them
         // only after the K barrier, which these threads reach after the reset.
@@ -700,57 +725,65 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
       const bool fast = __all_sync(0xffffffffu, amax >= 0x1p-90f && amax <= 0x1p+100f);
       const float s = fast ? div_corrected(amax, kE4M3Max, 1.0f / kE4M3Max) : (amax > 0.f ? amax / kE4M3Max : 1.f);
       if (tid == 0) p.scale[T][cur.bh * p.nblk + cur.blk] = s;
-      uint32_t pk[8];
-      if (fast) {
-        if (fwht) {
-          // Rotated rows (float32 butterflies, compared within one E4M3 step):
-          // x / (sqrt(d) s) as x times 448 / amax_u, from the hardware
-          // reciprocal (within a few float32 roundings of the quotient), so the
-          // path from the barrier to the codes is one reciprocal and products.
-          float r;
-          asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(amax_u));
-          const float yds = r * kE4M3Max;
-          const float2 y2 = make_float2(yds, yds);
+      const int row = cur.blk * kQuantRows + rib;
+      const bool have = row < p.N;
+      uint8_t* dst = p.dst[T] + (static_cast<size_t>(cur.bh) * p.N + (have ? row : 0)) * D;
+      // Codes are packed four to a word and stored as soon as a store's words
+      // are ready (rotated rows: lane g holds bytes 32 g ..; otherwise the four
+      // 8-byte runs 32 v + 8 g ..).
+      auto pack4 = [](float2 a, float2 b) -> uint32_t {
+        return __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3) |
+               (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(b, __NV_SATFINITE, __NV_E4M3)) << 16);
+      };
+      if (fast && fwht) {
+        // Rotated rows (float32 butterflies, compared within one E4M3 step):
+        // x / (sqrt(d) s) as x times 448 / amax_u, from the hardware reciprocal
+        // (within a few float32 roundings of the quotient), so the path from
+        // the barrier to the codes is one reciprocal and products.
+        float r;
+        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(amax_u));
+        const float yds = r * kE4M3Max;
+        const float2 y2 = make_float2(yds, yds);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint32_t lo = __nv_cvt_float2_to_fp8x2(fmul2(pair(x, 4 * q), y2), __NV_SATFINITE, __NV_E4M3);
-            const uint32_t hi = __nv_cvt_float2_to_fp8x2(fmul2(pair(x, 4 * q + 2), y2), __NV_SATFINITE, __NV_E4M3);
-            pk[q] = lo | (hi << 16);
-          }
-        } else {
-          const float y = __frcp_rn(s);
-          const float2 s2 = make_float2(s, s), ny2 = make_float2(-y, -y), y2 = make_float2(y, y);
+        for (int o = 0; o < 2; ++o) {
+          uint32_t w[4];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint32_t lo =
-                __nv_cvt_float2_to_fp8x2(div_by_scale2(pair(x, 4 * q), s2, ny2, y2), __NV_SATFINITE, __NV_E4M3);
-            const uint32_t hi = __nv_cvt_float2_to_fp8x2(div_by_scale2(pair(x, 4 * q + 2), s2, ny2, y2),
-                                                         __NV_SATFINITE, __NV_E4M3);
-            pk[q] = lo | (hi << 16);
+          for (int q = 0; q < 4; ++q) {
+            const int e = 16 * o + 4 * q;
+            w[q] = pack4(fmul2(pair(x, e), y2), fmul2(pair(x, e + 2), y2));
           }
+          if (have) reinterpret_cast<uint4*>(dst + 32 * g)[o] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else if (fast) {
+        const float y = __frcp_rn(s);
+        const float2 s2 = make_float2(s, s), ny2 = make_float2(-y, -y), y2 = make_float2(y, y);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int e = 8 * v;
+          const uint32_t w0 = pack4(div_by_scale2(pair(x, e), s2, ny2, y2), div_by_scale2(pair(x, e + 2), s2, ny2, y2));
+          const uint32_t w1 =
+              pack4(div_by_scale2(pair(x, e + 4), s2, ny2, y2), div_by_scale2(pair(x, e + 6), s2, ny2, y2));
+          if (have) *reinterpret_cast<uint2*>(dst + 32 * v + 8 * g) = make_uint2(w0, w1);
         }
       } else {
         const float c = fwht ? kInvSqrtD : 1.f;
+        uint32_t pk[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const float2 q01 = make_float2(__fdiv_rn(x[4 * q] * c, s), __fdiv_rn(x[4 * q + 1] * c, s));
           const float2 q23 = make_float2(__fdiv_rn(x[4 * q + 2] * c, s), __fdiv_rn(x[4 * q + 3] * c, s));
-          const uint32_t lo = __nv_cvt_float2_to_fp8x2(q01, __NV_SATFINITE, __NV_E4M3);
-          const uint32_t hi = __nv_cvt_float2_to_fp8x2(q23, __NV_SATFINITE, __NV_E4M3);
-          pk[q] = lo | (hi << 16);
+          pk[q] = pack4(q01, q23);
         }
-      }
-      const int row = cur.blk * kQuantRows + rib;
-      if (row < p.N) {
-        uint8_t* dst = p.dst[T] + (static_cast<size_t>(cur.bh) * p.N + row) * D;
-        if (fwht) {
-          uint4* out = reinterpret_cast<uint4*>(dst + 32 * g);
-          out[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          out[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        } else {
+        if (have) {
+          if (fwht) {
+            uint4* out = reinterpret_cast<uint4*>(dst + 32 * g);
+            out[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            out[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          } else {
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            *reinterpret_cast<uint2*>(dst + 32 * v + 8 * g) = make_uint2(pk[2 * v], pk[2 * v + 1]);
+            for (int v = 0; v < 4; ++v)
+              *reinterpret_cast<uint2*>(dst + 32 * v + 8 * g) = make_uint2(pk[2 * v], pk[2 * v + 1]);
+          }
         }
       }
     };
