@@ -327,7 +327,6 @@ constexpr int kStreamD = 128;
 constexpr int kStreamStageBytes = kQuantRows * kStreamD * 2;  // 32 KiB: one tensor of a unit
 constexpr int kStreamSlotStride = kPrepThreads * 16;          // bytes between a lane's 4 slots
 constexpr int kStreamSmemBytes = 3 * kStreamStageBytes;
-constexpr int kStreamMaskHeads = 32;  // sign masks of up to this many heads sit in shared memory
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
@@ -380,10 +379,24 @@ __device__ __forceinline__ float div_corrected(float a, float b, float y) {
   return fmaf(r, y, q0);
 }
 
-// Sign bit (bit 31) from bit 7 of byte `B` of w.
-template <int B>
-__device__ __forceinline__ uint32_t sign_of_byte(uint32_t w) {
-  return __byte_perm(w, 0u, 0x0444u | B << 12) & 0x80000000u;
+// Word i of a head's sign masks (signs: its d = 128 bytes, +1 = 0x01,
+// -1 = 0xff).  i < 64: lane g = i / 16, run v, pair q of the 16-bit input:
+// bits 15 and 31 are the signs of elements 32 v + 8 g + 2 q and + 1, XORed onto
+// the packed pair.  i >= 64 (rotary step, k = i mod 16): the product of the
+// two signs of rotary pair k of lane g at bit 31, XORed onto its sine
+// (half-split pairs: element 32 v + 8 g + j and + 64, k = 8 v + j; interleaved:
+// elements 32 v + 8 g + 2 q and + 1, k = 4 v + q).
+__device__ __forceinline__ uint32_t sign_mask_word(const int8_t* sg, int i, bool interleaved) {
+  const int g = (i >> 4) & 3;
+  if (i < 64) {
+    const int e = ((i >> 2) & 3) * 32 + g * 8 + (i & 3) * 2;
+    return (static_cast<uint32_t>(static_cast<uint8_t>(sg[e]) & 0x80u) << 8) |
+           (static_cast<uint32_t>(static_cast<uint8_t>(sg[e + 1]) & 0x80u) << 24);
+  }
+  const int k = i & 15;
+  const int ea = interleaved ? (k >> 2) * 32 + g * 8 + (k & 3) * 2 : (k >> 3) * 32 + g * 8 + (k & 7);
+  const int eb = interleaved ? ea + 1 : ea + 64;
+  return static_cast<uint32_t>((static_cast<uint8_t>(sg[ea]) ^ static_cast<uint8_t>(sg[eb])) & 0x80u) << 24;
 }
 
 // Lane indices of the thread, read through an empty volatile asm so that the
@@ -424,9 +437,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
   extern __shared__ __align__(128) uint8_t stream_smem[];
   // Block maxima (float bits) of Q, K and V, double-buffered by unit parity.
   __shared__ unsigned int blk_amax[2][3];
-  // Sign masks of the heads (H <= 32): word (h, g, v, q) holds the signs of
-  // elements 32 v + 8 g + 2 q and + 1 at bits 15 and 31, as the 16-bit pair.
-  __shared__ __align__(16) uint32_t mask_tab[kStreamMaskHeads * 64];
+  // The sign masks (sign_mask_word) of the head of this unit and of the next,
+  // by unit parity.
+  __shared__ __align__(16) uint32_t mask_tab[2][128];
   // Lane indices are re-read in every step (lane_ids), so that the per-lane
   // addresses derived from them are not kept live across the whole loop.
   const int tid0 = threadIdx.x;
@@ -434,16 +447,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
   const int begin = static_cast<int>(static_cast<long long>(n_units) * blockIdx.x / gridDim.x);
   const int end = static_cast<int>(static_cast<long long>(n_units) * (blockIdx.x + 1) / gridDim.x);
   const bool rotate = p.signs != nullptr;
-  const bool mask_smem = !ROPE && p.H <= kStreamMaskHeads;
   if (tid0 < 6) (&blk_amax[0][0])[tid0] = 0u;
-  if (rotate && mask_smem)
-    for (int i = tid0; i < p.H * 64; i += kPrepThreads) {
-      const int e0 = ((i >> 2) & 3) * 32 + ((i >> 4) & 3) * 8 + (i & 3) * 2;
-      const int8_t* sg = p.signs + (i >> 6) * D + e0;
-      mask_tab[i] = (static_cast<uint32_t>(static_cast<uint8_t>(sg[0]) & 0x80u) << 8) |
-                    (static_cast<uint32_t>(static_cast<uint8_t>(sg[1]) & 0x80u) << 24);
-    }
-  __syncthreads();
 
   // Row of this lane in a unit, as an index into the [B*H*N] rows (below 2^31:
   // the host takes the generic kernel otherwise); rows past N copy nothing.
@@ -470,6 +474,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
   cur.blk = begin / p.BH;
   cur.bh = begin - cur.blk * p.BH;
   cur.h = cur.bh % p.H;
+  constexpr int kMaskWords = ROPE ? 128 : 64;
+  if (rotate && tid0 < kMaskWords)
+    mask_tab[begin & 1][tid0] = sign_mask_word(p.signs + cur.h * D, tid0, p.rope_interleaved != 0);
+  __syncthreads();
   {
     uint32_t bytes;
     const int ridx = lane_row(cur, bytes);
@@ -502,16 +510,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
         const int r = lane_row(nx, bytes);
         issue(std::integral_constant<int, T - 1>(), u + 1 < end, r, bytes);
       }
-      const int h = cur.h;
       // Without the rotary step the widening and the first butterfly (element
       // bit 0) are one step: x0 + x1 and x0 - x1 straight from the 16-bit pair.
       const bool fused = fwht && !ROPE;
-      uint2 sw[4];  // sign bytes, where the masks are not in shared memory
-      if (fwht && !mask_smem) {
-        const int8_t* sg = p.signs + h * D + g * 8;
-#pragma unroll
-        for (int v = 0; v < 4; ++v) sw[v] = *reinterpret_cast<const uint2*>(sg + v * 32);
-      }
+      const uint32_t* mt = mask_tab[par] + g * 16;  // this lane's sign masks
       cp_async_wait<2>();  // this step's group; the next two steps' stay in flight
       if constexpr (T == 1) {
         // V of this unit (its copies are one group behind K's): its block
@@ -544,18 +546,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
           // widening and, through the sign of each sine, with the rotary step).
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            if (mask_smem) {
-              const uint4 m = *reinterpret_cast<const uint4*>(&mask_tab[(h * 4 + g) * 16 + v * 4]);
-              raw[v].x ^= m.x;
-              raw[v].y ^= m.y;
-              raw[v].z ^= m.z;
-              raw[v].w ^= m.w;
-            } else {
-              raw[v].x ^= __byte_perm(sw[v].x, 0u, 0x1404u) & 0x80008000u;
-              raw[v].y ^= __byte_perm(sw[v].x, 0u, 0x3424u) & 0x80008000u;
-              raw[v].z ^= __byte_perm(sw[v].y, 0u, 0x1404u) & 0x80008000u;
-              raw[v].w ^= __byte_perm(sw[v].y, 0u, 0x3424u) & 0x80008000u;
-            }
+            const uint4 m = *reinterpret_cast<const uint4*>(mt + v * 4);
+            raw[v].x ^= m.x;
+            raw[v].y ^= m.y;
+            raw[v].z ^= m.z;
+            raw[v].w ^= m.w;
           }
         }
 #pragma unroll
@@ -587,11 +582,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
               const float4 c4 = *reinterpret_cast<const float4*>(cr + 16 * v + 4 * g);
               float4 s4 = *reinterpret_cast<const float4*>(sr + 16 * v + 4 * g);
               if (fwht) {
-                const uint32_t px = sw[v].x ^ (sw[v].x >> 8), py = sw[v].y ^ (sw[v].y >> 8);
-                s4.x = __uint_as_float(__float_as_uint(s4.x) ^ sign_of_byte<0>(px));
-                s4.y = __uint_as_float(__float_as_uint(s4.y) ^ sign_of_byte<2>(px));
-                s4.z = __uint_as_float(__float_as_uint(s4.z) ^ sign_of_byte<0>(py));
-                s4.w = __uint_as_float(__float_as_uint(s4.w) ^ sign_of_byte<2>(py));
+                const uint4 m = *reinterpret_cast<const uint4*>(mt + 64 + v * 4);
+                s4.x = __uint_as_float(__float_as_uint(s4.x) ^ m.x);
+                s4.y = __uint_as_float(__float_as_uint(s4.y) ^ m.y);
+                s4.z = __uint_as_float(__float_as_uint(s4.z) ^ m.z);
+                s4.w = __uint_as_float(__float_as_uint(s4.w) ^ m.w);
               }
               const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, ss[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
@@ -606,15 +601,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
             // Pairs (i, i + d/2): element j of run v and of run v + 2, i = 32 v + 8 g + j.
 #pragma unroll
             for (int v = 0; v < 2; ++v) {
-              uint2 pr = make_uint2(0u, 0u);
-              if (fwht) pr = make_uint2(sw[v].x ^ sw[v + 2].x, sw[v].y ^ sw[v + 2].y);
 #pragma unroll
               for (int hh = 0; hh < 2; ++hh) {
                 const float4 c4 = *reinterpret_cast<const float4*>(cr + 32 * v + 8 * g + 4 * hh);
                 const float4 s4 = *reinterpret_cast<const float4*>(sr + 32 * v + 8 * g + 4 * hh);
-                const uint32_t pw = hh ? pr.y : pr.x;
-                const uint32_t m[4] = {sign_of_byte<0>(pw), sign_of_byte<1>(pw), sign_of_byte<2>(pw),
-                                       sign_of_byte<3>(pw)};
+                const uint4 mm = fwht ? *reinterpret_cast<const uint4*>(mt + 64 + 8 * v + 4 * hh) : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t m[4] = {mm.x, mm.y, mm.z, mm.w};
                 const float sv[4] = {s4.x, s4.y, s4.z, s4.w}, cv[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
                 for (int q = 0; q < 4; q += 2) {
@@ -784,6 +776,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
             for (int v = 0; v < 4; ++v)
               *reinterpret_cast<uint2*>(dst + 32 * v + 8 * g) = make_uint2(pk[2 * v], pk[2 * v + 1]);
           }
+        }
+      }
+      if constexpr (T == 0) {
+        // The next unit's sign masks into the other slot: its last reader,
+        // unit u - 1, finished before the previous K barrier, and this unit's
+        // K barrier publishes it.
+        if (rotate && tid < kMaskWords && u + 1 < end) {
+          const int hn = cur.h + 1 == p.H ? 0 : cur.h + 1;
+          mask_tab[par ^ 1][tid] = sign_mask_word(p.signs + hn * D, tid, p.rope_interleaved != 0);
         }
       }
     };
