@@ -46,6 +46,7 @@ struct PrepParams {
   const float* rsin;
   int rope_interleaved; // pairs (2i, 2i+1) if nonzero, else (i, i + d/2)
   int H, N, nblk, BH;
+  int codes_align32;    // Q and K code buffers start on 32-byte boundaries
 };
 
 // Correctly rounded x / s from y = RN(1 / s) with one FMA correction of the
@@ -343,6 +344,14 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                : "r"(addr)
                : "memory");
   return r;
+}
+
+// 32-byte store (the address is 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e,
+                                             uint32_t f, uint32_t g, uint32_t h) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d),
+               "r"(e), "r"(f), "r"(g), "r"(h)
+               : "memory");
 }
 
 // Per-halfword unsigned maximum of two packed pairs.
@@ -736,6 +745,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
         asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(amax_u));
         const float yds = r * kE4M3Max;
         const float2 y2 = make_float2(yds, yds);
+        uint32_t wk[4];
 #pragma unroll
         for (int o = 0; o < 2; ++o) {
           uint32_t w[4];
@@ -744,7 +754,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
             const int e = 16 * o + 4 * q;
             w[q] = pack4(fmul2(pair(x, e), y2), fmul2(pair(x, e + 2), y2));
           }
-          if (have) reinterpret_cast<uint4*>(dst + 32 * g)[o] = make_uint4(w[0], w[1], w[2], w[3]);
+          if (have) {
+            if (p.codes_align32) {
+              // Lane g's 32 code bytes in one store, so each store fills whole sectors.
+              if (o == 0) {
+                wk[0] = w[0]; wk[1] = w[1]; wk[2] = w[2]; wk[3] = w[3];
+              } else {
+                st_global_v8(dst + 32 * g, wk[0], wk[1], wk[2], wk[3], w[0], w[1], w[2], w[3]);
+              }
+            } else {
+              reinterpret_cast<uint4*>(dst + 32 * g)[o] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
         }
       } else if (fast) {
         const float y = __frcp_rn(s);
@@ -906,6 +927,7 @@ ATTN_EXPORT attn_status attn_fp8_prepare_rotary(const void* q, const void* k, co
   prm.N = N;
   prm.nblk = (N + kQuantRows - 1) / kQuantRows;
   prm.BH = B * H;
+  prm.codes_align32 = attn_internal::aligned(q8, 32) && attn_internal::aligned(k8, 32);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return in_dtype == ATTN_BF16 ? run_prepare<true>(prm, d, per_tensor, s)
                                : run_prepare<false>(prm, d, per_tensor, s);

@@ -324,6 +324,24 @@ def test_prepare_rotation_many_items_per_cta(rope, dtype):
     assert attn.device_status() == attn.ATTN_OK
 
 
+def test_prepare_code_buffers_off_32_byte_boundaries():
+    """Code buffers that start 16 bytes past a 32-byte boundary take 16-byte
+    stores instead of 32-byte ones: the same codes and scales."""
+    B, H, N, d = 2, 4, 640, 128
+    q, k, v = (t.cuda() for t in synth.outlier_inputs(B, H, N, d, "bf16", seed=15))
+    signs = synth.hadamard_signs(H, d, seed=15).cuda()
+    ref = attn.fp8_prepare(q, k, v, signs=signs)
+    n = B * H * N * d
+    raw = [torch.empty(n + 64, dtype=torch.uint8, device="cuda") for _ in range(3)]
+    codes = [r[16:16 + n].view(B, H, N, d) for r in raw]
+    assert all(c.data_ptr() % 32 == 16 for c in codes)
+    scales = [torch.empty((B, H, N // 128), dtype=torch.float32, device="cuda") for _ in range(3)]
+    out = attn.fp8_prepare(q, k, v, signs=signs, out=codes + scales)
+    torch.cuda.synchronize()
+    for a, b in zip(ref, out):
+        assert torch.equal(a, b)
+
+
 @pytest.mark.parametrize("d", PREP_D)
 @pytest.mark.parametrize("interleaved", [False, True])
 @pytest.mark.parametrize("rotate", [False, True])
