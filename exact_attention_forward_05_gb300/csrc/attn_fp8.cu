@@ -328,6 +328,11 @@ constexpr int kStreamD = 128;
 constexpr int kStreamStageBytes = kQuantRows * kStreamD * 2;  // 32 KiB: one tensor of a unit
 constexpr int kStreamSlotStride = kPrepThreads * 16;          // bytes between a lane's 4 slots
 constexpr int kStreamSmemBytes = 3 * kStreamStageBytes;
+// Rotary tables of the current 128-row block in shared memory (rotary kernel,
+// one CTA per SM): per row and lane g, the 16 cos and 16 sin entries the lane
+// uses, as 8 float4 in the order it reads them, XOR-swizzled within the lane's
+// 128 bytes so that a warp's reads are conflict-free.
+constexpr int kStreamTableBytes = kQuantRows * 4 * 8 * 16;  // 64 KiB
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
@@ -440,7 +445,7 @@ __device__ __forceinline__ void next_unit(PrepUnit& u, int BH, int H) {
 }
 
 template <bool BF16IN, bool ROPE>
-__global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(const PrepParams p, int n_units) {
+__global__ void __launch_bounds__(kPrepThreads, ROPE ? 1 : 2) fp8_prepare_stream_kernel(const PrepParams p, int n_units) {
   constexpr int D = kStreamD, VPL = D / 4;
   constexpr float kInvSqrtD = 0.08838834764831845f;
   extern __shared__ __align__(128) uint8_t stream_smem[];
@@ -495,10 +500,40 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
     issue(std::integral_constant<int, 1>(), live, ridx, bytes);
   }
 
+  // Rotary kernel: float4 k of lane block lb = 4 r + g (row r of the block)
+  // holds cos (k even) or sin (k odd) entries of quad k / 2: half-split pairs
+  // i = 32 v + 8 g + 4 hh + 0..3 with k / 2 = 2 v + hh; interleaved pairs
+  // i = 16 v + 4 g + 0..3 with k / 2 = v.
+  const uint32_t tbase = sbase + 3 * kStreamStageBytes;
+  auto load_tables = [&](int blk) {
+    const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int f = tid0 + kPrepThreads * i, lb = f >> 3, k = f & 7, gg = lb & 3;
+      const int row = blk * kQuantRows + (lb >> 2);
+      const int quad = k >> 1;
+      const int idx = p.rope_interleaved ? 16 * quad + 4 * gg : 32 * (quad >> 1) + 8 * gg + 4 * (quad & 1);
+      const float* tab = (k & 1) ? p.rsin : p.rcos;
+      const float4 val = row < p.N ? *reinterpret_cast<const float4*>(tab + static_cast<size_t>(row) * (D / 2) + idx)
+                                   : zero4;
+      st_shared_v4(tbase + (lb * 8 + (k ^ (lb & 7))) * 16, __float_as_uint(val.x), __float_as_uint(val.y),
+                   __float_as_uint(val.z), __float_as_uint(val.w));
+    }
+  };
+  int table_blk = -1;
+
   for (int u = begin; u < end; ++u) {
     const int par = u & 1;
+    if constexpr (ROPE) {
+      if (cur.blk != table_blk) {
+        // The previous block's tables were last read before the previous K barrier.
+        load_tables(cur.blk);
+        __syncthreads();
+        table_blk = cur.blk;
+      }
+    }
     // Per-lane values are recomputed where they are used (registers are the
-    // limit at two CTAs per SM).
+    // limit at two CTAs per SM: 64 per thread).
 
     auto step = [&](auto tc) {
       constexpr int T = decltype(tc)::value;
@@ -577,57 +612,58 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fp8_prepare_stream_kernel(con
         }
       }
       if constexpr (QK && ROPE) {
-        const int row = cur.blk * kQuantRows + rib;
-        if (row < p.N) {
-          // With the signs already on the inputs, pair (a, b) with signs (sa, sb)
-          // takes the rotation with sin * sa * sb, which gives sa (a c - b s) and
-          // sb (a s + b c), bit for bit (rounding is odd-symmetric).
-          const float* cr = p.rcos + static_cast<size_t>(row) * (D / 2);
-          const float* sr = p.rsin + static_cast<size_t>(row) * (D / 2);
-          if (p.rope_interleaved) {
-            // Pairs (2i, 2i+1): elements j, j+1 of run v, i = 16 v + 4 g + j / 2.
+        // With the signs already on the inputs, pair (a, b) with signs (sa, sb)
+        // takes the rotation with sin * sa * sb, which gives sa (a c - b s) and
+        // sb (a s + b c), bit for bit (rounding is odd-symmetric).  Table
+        // entries from the block's shared copy (zero past N).
+        const int lb = rib * 4 + g;
+        auto tab4 = [&](int k) -> float4 {
+          const uint4 r = ld_shared_v4(tbase + (lb * 8 + (k ^ (lb & 7))) * 16);
+          return make_float4(__uint_as_float(r.x), __uint_as_float(r.y), __uint_as_float(r.z), __uint_as_float(r.w));
+        };
+        if (p.rope_interleaved) {
+          // Pairs (2i, 2i+1): elements j, j+1 of run v, i = 16 v + 4 g + j / 2.
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const float4 c4 = *reinterpret_cast<const float4*>(cr + 16 * v + 4 * g);
-              float4 s4 = *reinterpret_cast<const float4*>(sr + 16 * v + 4 * g);
-              if (fwht) {
-                const uint4 m = *reinterpret_cast<const uint4*>(mt + 64 + v * 4);
-                s4.x = __uint_as_float(__float_as_uint(s4.x) ^ m.x);
-                s4.y = __uint_as_float(__float_as_uint(s4.y) ^ m.y);
-                s4.z = __uint_as_float(__float_as_uint(s4.z) ^ m.z);
-                s4.w = __uint_as_float(__float_as_uint(s4.w) ^ m.w);
-              }
-              const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, ss[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const int e = 8 * v + 2 * q;
-                const float a = x[e], b = x[e + 1];
-                x[e] = fmaf(a, cc[q], -(b * ss[q]));
-                x[e + 1] = fmaf(a, ss[q], b * cc[q]);
-              }
+          for (int v = 0; v < 4; ++v) {
+            const float4 c4 = tab4(2 * v);
+            float4 s4 = tab4(2 * v + 1);
+            if (fwht) {
+              const uint4 m = *reinterpret_cast<const uint4*>(mt + 64 + v * 4);
+              s4.x = __uint_as_float(__float_as_uint(s4.x) ^ m.x);
+              s4.y = __uint_as_float(__float_as_uint(s4.y) ^ m.y);
+              s4.z = __uint_as_float(__float_as_uint(s4.z) ^ m.z);
+              s4.w = __uint_as_float(__float_as_uint(s4.w) ^ m.w);
             }
-          } else {
-            // Pairs (i, i + d/2): element j of run v and of run v + 2, i = 32 v + 8 g + j.
+            const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, ss[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
-            for (int v = 0; v < 2; ++v) {
+            for (int q = 0; q < 4; ++q) {
+              const int e = 8 * v + 2 * q;
+              const float a = x[e], b = x[e + 1];
+              x[e] = fmaf(a, cc[q], -(b * ss[q]));
+              x[e + 1] = fmaf(a, ss[q], b * cc[q]);
+            }
+          }
+        } else {
+          // Pairs (i, i + d/2): element j of run v and of run v + 2, i = 32 v + 8 g + j.
 #pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                const float4 c4 = *reinterpret_cast<const float4*>(cr + 32 * v + 8 * g + 4 * hh);
-                const float4 s4 = *reinterpret_cast<const float4*>(sr + 32 * v + 8 * g + 4 * hh);
-                const uint4 mm = fwht ? *reinterpret_cast<const uint4*>(mt + 64 + 8 * v + 4 * hh) : make_uint4(0u, 0u, 0u, 0u);
-                const uint32_t m[4] = {mm.x, mm.y, mm.z, mm.w};
-                const float sv[4] = {s4.x, s4.y, s4.z, s4.w}, cv[4] = {c4.x, c4.y, c4.z, c4.w};
+          for (int v = 0; v < 2; ++v) {
 #pragma unroll
-                for (int q = 0; q < 4; q += 2) {
-                  const int e = 8 * v + 4 * hh + q;
-                  const float2 sp = make_float2(__uint_as_float(__float_as_uint(sv[q]) ^ m[q]),
-                                                __uint_as_float(__float_as_uint(sv[q + 1]) ^ m[q + 1]));
-                  const float2 sn = make_float2(-sp.x, -sp.y);
-                  const float2 a = pair(x, e), b = pair(x, e + 16);
-                  const float2 c2 = make_float2(cv[q], cv[q + 1]);
-                  put(x, e, ffma2(b, sn, fmul2(a, c2)));
-                  put(x, e + 16, ffma2(a, sp, fmul2(b, c2)));
-                }
+            for (int hh = 0; hh < 2; ++hh) {
+              const float4 c4 = tab4(2 * (2 * v + hh));
+              const float4 s4 = tab4(2 * (2 * v + hh) + 1);
+              const uint4 mm = fwht ? *reinterpret_cast<const uint4*>(mt + 64 + 8 * v + 4 * hh) : make_uint4(0u, 0u, 0u, 0u);
+              const uint32_t m[4] = {mm.x, mm.y, mm.z, mm.w};
+              const float sv[4] = {s4.x, s4.y, s4.z, s4.w}, cv[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+              for (int q = 0; q < 4; q += 2) {
+                const int e = 8 * v + 4 * hh + q;
+                const float2 sp = make_float2(__uint_as_float(__float_as_uint(sv[q]) ^ m[q]),
+                                              __uint_as_float(__float_as_uint(sv[q + 1]) ^ m[q + 1]));
+                const float2 sn = make_float2(-sp.x, -sp.y);
+                const float2 a = pair(x, e), b = pair(x, e + 16);
+                const float2 c2 = make_float2(cv[q], cv[q + 1]);
+                put(x, e, ffma2(b, sn, fmul2(a, c2)));
+                put(x, e + 16, ffma2(a, sp, fmul2(b, c2)));
               }
             }
           }
@@ -825,24 +861,26 @@ __global__ void fp8_finalize_scale_kernel(float* q_scale, float* k_scale, float*
   }
 }
 
-// d = 128, per-block scales: the streaming pre-pass, two CTAs per SM.
+// d = 128, per-block scales: the streaming pre-pass (two CTAs per SM; the rotary kernel one).
 template <bool BF16IN, bool ROPE>
 attn_status run_prepare_stream(const PrepParams& prm, cudaStream_t s) {
+  constexpr int smem = kStreamSmemBytes + (ROPE ? kStreamTableBytes : 0);
   static int configured_for[64] = {0};  // per device: dynamic shared memory attribute set
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return attn_internal::cuda_status(e);
   if (dev >= 64 || !configured_for[dev]) {
     e = cudaFuncSetAttribute(fp8_prepare_stream_kernel<BF16IN, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kStreamSmemBytes);
+                             smem);
     if (e != cudaSuccess) return attn_internal::cuda_status(e);
     if (dev < 64) configured_for[dev] = 1;
   }
   const int sms = attn_internal::sm_count();
   if (sms <= 0) return ATTN_ERR_CUDA;
   const int n_units = prm.BH * prm.nblk;  // (row block, head) units, three steps each
-  const int grid = n_units < 2 * sms ? n_units : 2 * sms;
-  fp8_prepare_stream_kernel<BF16IN, ROPE><<<grid, kPrepThreads, kStreamSmemBytes, s>>>(prm, n_units);
+  const int per_sm = ROPE ? 1 : 2;  // the rotary kernel keeps its block's tables in shared memory
+  const int grid = n_units < per_sm * sms ? n_units : per_sm * sms;
+  fp8_prepare_stream_kernel<BF16IN, ROPE><<<grid, kPrepThreads, smem, s>>>(prm, n_units);
   return attn_internal::cuda_status(cudaGetLastError());
 }
 
