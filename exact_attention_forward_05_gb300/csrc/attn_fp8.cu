@@ -413,6 +413,10 @@ __device__ __forceinline__ uint32_t sign_mask_word(const int8_t* sg, int i, bool
   return static_cast<uint32_t>((static_cast<uint8_t>(sg[ea]) ^ static_cast<uint8_t>(sg[eb])) & 0x80u) << 24;
 }
 
+// Position of sign_mask_word i in the shared table: lane g's input masks at
+// g * 36, its rotary sine masks at g * 36 + 16.
+__device__ __forceinline__ int mask_slot(int i) { return ((i >> 4) & 3) * 36 + (i >= 64 ? 16 : 0) + (i & 15); }
+
 // Lane indices of the thread, read through an empty volatile asm so that the
 // compiler re-derives them (and the addresses built from them) where they are
 // used instead of holding them in registers for the whole kernel.
@@ -453,7 +457,9 @@ __global__ void __launch_bounds__(kPrepThreads, ROPE ? 1 : 2) fp8_prepare_stream
   __shared__ unsigned int blk_amax[2][3];
   // The sign masks (sign_mask_word) of the head of this unit and of the next,
   // by unit parity.
-  __shared__ __align__(16) uint32_t mask_tab[2][128];
+  // Lane g's 32 words at g * 36 (16-byte aligned, no bank conflicts between the
+  // four lanes of a row).
+  __shared__ __align__(16) uint32_t mask_tab[2][4 * 36];
   // Lane indices are re-read in every step (lane_ids), so that the per-lane
   // addresses derived from them are not kept live across the whole loop.
   const int tid0 = threadIdx.x;
@@ -490,7 +496,7 @@ __global__ void __launch_bounds__(kPrepThreads, ROPE ? 1 : 2) fp8_prepare_stream
   cur.h = cur.bh % p.H;
   constexpr int kMaskWords = ROPE ? 128 : 64;
   if (rotate && tid0 < kMaskWords)
-    mask_tab[begin & 1][tid0] = sign_mask_word(p.signs + cur.h * D, tid0, p.rope_interleaved != 0);
+    mask_tab[begin & 1][mask_slot(tid0)] = sign_mask_word(p.signs + cur.h * D, tid0, p.rope_interleaved != 0);
   __syncthreads();
   {
     uint32_t bytes;
@@ -557,7 +563,7 @@ __global__ void __launch_bounds__(kPrepThreads, ROPE ? 1 : 2) fp8_prepare_stream
       // Without the rotary step the widening and the first butterfly (element
       // bit 0) are one step: x0 + x1 and x0 - x1 straight from the 16-bit pair.
       const bool fused = fwht && !ROPE;
-      const uint32_t* mt = mask_tab[par] + g * 16;  // this lane's sign masks
+      const uint32_t* mt = mask_tab[par] + g * 36;  // this lane's sign masks
       cp_async_wait<2>();  // this step's group; the next two steps' stay in flight
       if constexpr (T == 1) {
         // V of this unit (its copies are one group behind K's): its block
@@ -628,7 +634,7 @@ __global__ void __launch_bounds__(kPrepThreads, ROPE ? 1 : 2) fp8_prepare_stream
             const float4 c4 = tab4(2 * v);
             float4 s4 = tab4(2 * v + 1);
             if (fwht) {
-              const uint4 m = *reinterpret_cast<const uint4*>(mt + 64 + v * 4);
+              const uint4 m = *reinterpret_cast<const uint4*>(mt + 16 + v * 4);
               s4.x = __uint_as_float(__float_as_uint(s4.x) ^ m.x);
               s4.y = __uint_as_float(__float_as_uint(s4.y) ^ m.y);
               s4.z = __uint_as_float(__float_as_uint(s4.z) ^ m.z);
@@ -651,7 +657,7 @@ __global__ void __launch_bounds__(kPrepThreads, ROPE ? 1 : 2) fp8_prepare_stream
             for (int hh = 0; hh < 2; ++hh) {
               const float4 c4 = tab4(2 * (2 * v + hh));
               const float4 s4 = tab4(2 * (2 * v + hh) + 1);
-              const uint4 mm = fwht ? *reinterpret_cast<const uint4*>(mt + 64 + 8 * v + 4 * hh) : make_uint4(0u, 0u, 0u, 0u);
+              const uint4 mm = fwht ? *reinterpret_cast<const uint4*>(mt + 16 + 8 * v + 4 * hh) : make_uint4(0u, 0u, 0u, 0u);
               const uint32_t m[4] = {mm.x, mm.y, mm.z, mm.w};
               const float sv[4] = {s4.x, s4.y, s4.z, s4.w}, cv[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
@@ -841,7 +847,7 @@ __global__ void __launch_bounds__(kPrepThreads, ROPE ? 1 : 2) fp8_prepare_stream
         // K barrier publishes it.
         if (rotate && tid < kMaskWords && u + 1 < end) {
           const int hn = cur.h + 1 == p.H ? 0 : cur.h + 1;
-          mask_tab[par ^ 1][tid] = sign_mask_word(p.signs + hn * D, tid, p.rope_interleaved != 0);
+          mask_tab[par ^ 1][mask_slot(tid)] = sign_mask_word(p.signs + hn * D, tid, p.rope_interleaved != 0);
         }
       }
     };
