@@ -448,7 +448,7 @@ __device__ __forceinline__ void next_unit(PrepUnit& u, int BH, int H) {
   }
 }
 
-template <bool BF16IN, bool ROPE>
+template <bool BF16IN, bool ROPE, bool ROTATE>
 __global__ void __launch_bounds__(kPrepThreads, ROPE ? 1 : 2) fp8_prepare_stream_kernel(const PrepParams p, int n_units) {
   constexpr int D = kStreamD, VPL = D / 4;
   constexpr float kInvSqrtD = 0.08838834764831845f;
@@ -466,7 +466,7 @@ __global__ void __launch_bounds__(kPrepThreads, ROPE ? 1 : 2) fp8_prepare_stream
   const uint32_t sbase = smem_u32(stream_smem);
   const int begin = static_cast<int>(static_cast<long long>(n_units) * blockIdx.x / gridDim.x);
   const int end = static_cast<int>(static_cast<long long>(n_units) * (blockIdx.x + 1) / gridDim.x);
-  const bool rotate = p.signs != nullptr;
+  constexpr bool rotate = ROTATE;  // the caller passed signs
   if (tid0 < 6) (&blk_amax[0][0])[tid0] = 0u;
 
   // Row of this lane in a unit, as an index into the [B*H*N] rows (below 2^31:
@@ -868,7 +868,7 @@ __global__ void fp8_finalize_scale_kernel(float* q_scale, float* k_scale, float*
 }
 
 // d = 128, per-block scales: the streaming pre-pass (two CTAs per SM; the rotary kernel one).
-template <bool BF16IN, bool ROPE>
+template <bool BF16IN, bool ROPE, bool ROTATE>
 attn_status run_prepare_stream(const PrepParams& prm, cudaStream_t s) {
   constexpr int smem = kStreamSmemBytes + (ROPE ? kStreamTableBytes : 0);
   static int configured_for[64] = {0};  // per device: dynamic shared memory attribute set
@@ -876,7 +876,7 @@ attn_status run_prepare_stream(const PrepParams& prm, cudaStream_t s) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return attn_internal::cuda_status(e);
   if (dev >= 64 || !configured_for[dev]) {
-    e = cudaFuncSetAttribute(fp8_prepare_stream_kernel<BF16IN, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(fp8_prepare_stream_kernel<BF16IN, ROPE, ROTATE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem);
     if (e != cudaSuccess) return attn_internal::cuda_status(e);
     if (dev < 64) configured_for[dev] = 1;
@@ -886,7 +886,7 @@ attn_status run_prepare_stream(const PrepParams& prm, cudaStream_t s) {
   const int n_units = prm.BH * prm.nblk;  // (row block, head) units, three steps each
   const int per_sm = ROPE ? 1 : 2;  // the rotary kernel keeps its block's tables in shared memory
   const int grid = n_units < per_sm * sms ? n_units : per_sm * sms;
-  fp8_prepare_stream_kernel<BF16IN, ROPE><<<grid, kPrepThreads, smem, s>>>(prm, n_units);
+  fp8_prepare_stream_kernel<BF16IN, ROPE, ROTATE><<<grid, kPrepThreads, smem, s>>>(prm, n_units);
   return attn_internal::cuda_status(cudaGetLastError());
 }
 
@@ -895,7 +895,11 @@ attn_status run_prepare_d(const PrepParams& prm, int per_tensor, cudaStream_t s)
   const dim3 grid(static_cast<unsigned>(prm.BH) * prm.nblk, 3);
   if constexpr (D == kStreamD) {
     if (!per_tensor && static_cast<long long>(prm.BH) * prm.N < 0x7fffffffll)
-      return prm.rcos != nullptr ? run_prepare_stream<BF16IN, true>(prm, s) : run_prepare_stream<BF16IN, false>(prm, s);
+    {
+      const bool rope = prm.rcos != nullptr, rot = prm.signs != nullptr;
+      if (rope) return rot ? run_prepare_stream<BF16IN, true, true>(prm, s) : run_prepare_stream<BF16IN, true, false>(prm, s);
+      return rot ? run_prepare_stream<BF16IN, false, true>(prm, s) : run_prepare_stream<BF16IN, false, false>(prm, s);
+    }
   }
   if (!per_tensor) {
     fp8_prepare_kernel<D, BF16IN, PREP_BLOCK><<<grid, kPrepThreads, 0, s>>>(prm);
