@@ -810,14 +810,22 @@ __global__ void __launch_bounds__(kPrepThreads, ROPE ? 1 : 2) fp8_prepare_stream
           }
         }
       } else if (fast) {
+        // -RN(x / s) by the FMA correction taken on the negated product, then
+        // the codes' sign bits flipped (E4M3 is sign-magnitude and its rounding
+        // symmetric): one product fewer per pair than div_by_scale2, zeros keep
+        // their sign (x = -0: -q = +0, code 0x80).
         const float y = __frcp_rn(s);
-        const float2 s2 = make_float2(s, s), ny2 = make_float2(-y, -y), y2 = make_float2(y, y);
+        const float2 s2 = make_float2(s, s), ny2 = make_float2(-y, -y);
+        auto neg_q = [&](int e) {
+          const float2 xv = pair(x, e);
+          const float2 q0n = fmul2(xv, ny2);
+          return ffma2(ffma2(q0n, s2, xv), ny2, q0n);
+        };
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           const int e = 8 * v;
-          const uint32_t w0 = pack4(div_by_scale2(pair(x, e), s2, ny2, y2), div_by_scale2(pair(x, e + 2), s2, ny2, y2));
-          const uint32_t w1 =
-              pack4(div_by_scale2(pair(x, e + 4), s2, ny2, y2), div_by_scale2(pair(x, e + 6), s2, ny2, y2));
+          const uint32_t w0 = pack4(neg_q(e), neg_q(e + 2)) ^ 0x80808080u;
+          const uint32_t w1 = pack4(neg_q(e + 4), neg_q(e + 6)) ^ 0x80808080u;
           if (have) *reinterpret_cast<uint2*>(dst + 32 * v + 8 * g) = make_uint2(w0, w1);
         }
       } else {
