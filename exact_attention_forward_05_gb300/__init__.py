@@ -285,10 +285,11 @@ FP8_BLOCK = 128  # rows per quantisation scale block
 
 def fp8_prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, signs: torch.Tensor | None = None,
                 per_tensor: bool = False, stream=None, out=None, rope=None, rope_interleaved: bool = False):
-    """FP8 pre-pass on CUDA tensors [B, H, N, 128] (fp16 or bf16): rotary
-    embedding of Q and K (when ``rope`` = (cos, sin), float32 [N, 64] CUDA
-    tables; pairs (2i, 2i+1) if ``rope_interleaved`` else (i, i + 64)), then
-    their random-sign Hadamard rotation (when ``signs`` [H, 128] int8 is given)
+    """FP8 pre-pass on CUDA tensors [B, H, N, d], d = 64, 128 or 256 (fp16 or
+    bf16): rotary embedding of Q and K (when ``rope`` = (cos, sin), float32
+    [N, d/2] CUDA tables; pairs (2i, 2i+1) if ``rope_interleaved`` else
+    (i, i + d/2)), then
+    their random-sign Hadamard rotation (when ``signs`` [H, d] int8 is given)
     and E4M3 quantisation with one float32 scale per 128 rows of a head (or one
     per tensor).  Returns (q8, k8, v8, q_scale, k_scale, v_scale); the codes are
     uint8 tensors [B, H, N, 128].  ``out`` may pass those six tensors in."""
