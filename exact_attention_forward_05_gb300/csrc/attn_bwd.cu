@@ -91,12 +91,19 @@ struct BCfg {
   // One CTA per SM (TMEM is allocated whole): at least 115 KiB of shared memory.
   static constexpr int SMEM_BYTES = USED > 115 * 1024 ? USED : 115 * 1024;
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-  // TMEM columns: S^T (later P^T in its first 64, then the dQ partial), dP^T
-  // (later dS^T in its first 64), dV, dK.
+  // TMEM columns: S^T (later P^T in its columns 0-31 and 96-127, then the dQ
+  // partial), dP^T (later dS^T in the same columns of its own), dV, dK.
   static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D, TMEM_COLS = 512;
   static_assert(256 + 2 * D <= 512, "S^T, dP^T, dV and dK fit in TMEM");
-  static constexpr int THREADS = 192;  // warps 0-3 compute, 4 load, 5 MMA
-  static constexpr int LOAD_WARP = 4, MMA_WARP = 5;
+  // Warps 0-7 compute (warp w: TMEM lanes 32 (w mod 4) .. + 31, column half
+  // w / 4 of every 128-column pass), 8 load, 9 MMA.
+  static constexpr int COMPUTE = 256;
+  // Launched as 384 threads x 168 registers; the third warpgroup (load, MMA
+  // and two idle warps) gives registers to the two compute warpgroups with
+  // setmaxnreg: 2 x 128 x 200 + 128 x 88 = 62464 <= 384 x 168 = 64512.
+  static constexpr int THREADS = COMPUTE + 128;
+  static constexpr int LOAD_WARP = 8, MMA_WARP = 9;
+  static constexpr int COMPUTE_REGS = 200, OTHER_REGS = 88;
 };
 
 struct BwdParams {
@@ -172,7 +179,7 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < C::NBARS; ++b)
-      mbar_init(BAR(b), (b == C::B_P_READY || b == C::B_DQ_READ || b == C::B_EPI_DONE) ? 4 : 1);
+      mbar_init(BAR(b), (b == C::B_P_READY || b == C::B_DQ_READ || b == C::B_EPI_DONE) ? C::COMPUTE / 32 : 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -193,6 +200,10 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, &g_status_word, p.timeout_ns};
 
+  // The register budget changes inside each warpgroup's own branch, so that
+  // the compiler allocates every role's code against its own budget.
+  if (warp >= C::LOAD_WARP) {
+  setmaxnreg_dec<C::OTHER_REGS>();
   if (warp == C::LOAD_WARP) {
     // ---------------------------------------------------------------- loads
     if (lane == 0) {
@@ -254,9 +265,9 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
       auto mma_tmem_a = [&](uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, bool acc) {
         const uint32_t b0 = desc_sw128_lo(b_smem, C::CHUNK_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < kB / 16; ++kk)
-          mma_ts_w(d_tmem, a_tmem + kk * 8, b0 + ((kk * 16 * 128) >> 4), HI, ID_ACC, (acc || kk > 0) ? 1u : 0u,
-                   false);
+        for (int kk = 0; kk < kB / 16; ++kk)  // 16-bit columns 0..31 and 96..127 (queries 0..63, 64..127)
+          mma_ts_w(d_tmem, a_tmem + kk * 8 + (kk >= kB / 32 ? 64 : 0), b0 + ((kk * 16 * 128) >> 4), HI, ID_ACC,
+                   (acc || kk > 0) ? 1u : 0u, false);
       };
       for (int r = 0; ok && r * G < p.num_units; ++r) {
         const int u = unit_of(r);
@@ -309,10 +320,13 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
       mma_commit(BAR(C::B_MMA_DONE));
       drain(BAR(C::B_MMA_DONE), 0, 100000000ull);
     }
+  }
   } else {
-    // ------------------------------------------------ compute (4 warps, 128 threads)
-    const int row = warp * 32 + lane;  // TMEM lane: key row of S^T, dP^T, dV, dK; query row of dQ
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    setmaxnreg_inc<C::COMPUTE_REGS>();
+    // ------------------------------------------------ compute (8 warps, 256 threads)
+    const int quad = warp & 3, half = warp >> 2;  // TMEM lane quadrant, column half
+    const int row = quad * 32 + lane;  // TMEM lane: key row of S^T, dP^T, dV, dK; query row of dQ
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     uint32_t sp_it = 0, dq_it = 0;
     bool ok = true;
     constexpr float kLog2e = 1.4426950408889634f;
@@ -338,23 +352,24 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
         // Stage this block's values for the four warps.  The dS buffer below
         // is also the staging of the last dQ reduce: it must have been read.
         if (threadIdx.x == 0) bulk_wait_read_all();
-        if (bar_red_or(1, 128, !ok)) { ok = false; break; }
-        const int q_row = i * kB + row;
-        lse_s[row] = next_l2;
-        d_s[row] = next_d;
-        bar_sync_n(1, 128);
-        fetch(i + 1, next_l2, next_d);
+        if (bar_red_or(1, C::COMPUTE, !ok)) { ok = false; break; }
+        if (half == 0) {  // the first four warps stage the block's lse and D
+          lse_s[row] = next_l2;
+          d_s[row] = next_d;
+        }
+        bar_sync_n(1, C::COMPUTE);
+        if (half == 0) fetch(i + 1, next_l2, next_d);
         if (!(ok = mbar_wait_warp(BAR(C::B_SP_FULL), sp_it & 1u, wc, attn_internal::kStatusTimeoutSoftmax))) {
-          bar_red_or(2, 128, true);
+          bar_red_or(2, C::COMPUTE, true);
           break;
         }
         ++sp_it;
         tc_fence_after();
         const bool diag = p.causal && i == j;
-        // 64 queries at a time: S^T and dP^T columns of two 32-query chunks
+        // This warp's 64 queries: S^T and dP^T columns of two 32-query chunks
         // loaded under one wait; lse and D read four at a time.
-#pragma unroll 1
-        for (int c2 = 0; c2 < kB / 64; ++c2) {
+        {
+          const int c2 = half;
           uint32_t s[2][32], dp[2][32];
           tmem_ld32(lane_base + C::TM_S + 64 * c2, s[0]);
           tmem_ld32(lane_base + C::TM_S + 64 * c2 + 32, s[1]);
@@ -387,8 +402,11 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
               dk16[2 * t4] = pack16<BF16>(dsv[0], dsv[1]);
               dk16[2 * t4 + 1] = pack16<BF16>(dsv[2], dsv[3]);
             }
-            tmem_st16(lane_base + C::TM_S + 16 * c, pk);
-            tmem_st16(lane_base + C::TM_DP + 16 * c, dk16);
+            // The second half of the warps writes its 16-bit values into its own
+            // loaded columns (96 .. 127), never into columns the first half may
+            // still be reading; the products take that gap into account.
+            tmem_st16(lane_base + C::TM_S + 16 * c + 64 * half, pk);
+            tmem_st16(lane_base + C::TM_DP + 16 * c + 64 * half, dk16);
             // dS into shared memory: row `row`, queries 32c .. 32c + 31, 128-byte
             // swizzled spans of 64 queries (the layout a tiled copy would give).
             const uint32_t span = sDS + static_cast<uint32_t>(c >> 1) * C::CHUNK_BYTES + static_cast<uint32_t>(row) * 128u;
@@ -406,33 +424,29 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
         if (lane == 0) mbar_arrive(BAR(C::B_P_READY));
         // dQ partial of this query block: TMEM lane = query row.
         const bool got = mbar_wait_warp(BAR(C::B_DQ_FULL), dq_it & 1u, wc, attn_internal::kStatusTimeoutSoftmax);
-        if (bar_red_or(2, 128, !got)) { ok = false; break; }
+        if (bar_red_or(2, C::COMPUTE, !got)) { ok = false; break; }
         ++dq_it;
         tc_fence_after();
         // 64 columns at a time through the dS buffer (free: the dQ product
-        // has read it), two 32-float 128-byte swizzled boxes, reduce-added
-        // into the float32 accumulator (rows past N are skipped by the copy).
+        // has read it): each half of the warps stages one 32-float 128-byte
+        // swizzled box, reduce-added into the float32 accumulator (rows past N
+        // are skipped by the copy).
 #pragma unroll 1
         for (int rnd = 0; rnd < D / 64; ++rnd) {
-          uint32_t v[2][32];
-          tmem_ld32(lane_base + C::TM_S + 64 * rnd, v[0]);
-          tmem_ld32(lane_base + C::TM_S + 64 * rnd + 32, v[1]);
-          tmem_wait_ld(v[0]);
-          reg_pin(v[1]);
+          uint32_t v[32];
+          tmem_ld32(lane_base + C::TM_S + 64 * rnd + 32 * half, v);
+          tmem_wait_ld(v);
           if (rnd > 0) {
             if (threadIdx.x == 0) bulk_wait_read_all();
-            bar_sync_n(1, 128);
+            bar_sync_n(1, C::COMPUTE);
           }
+          const uint32_t box_row = sDS + static_cast<uint32_t>(half) * C::CHUNK_BYTES + static_cast<uint32_t>(row) * 128u;
 #pragma unroll
-          for (int b = 0; b < 2; ++b) {
-            const uint32_t box_row = sDS + static_cast<uint32_t>(b) * C::CHUNK_BYTES + static_cast<uint32_t>(row) * 128u;
-#pragma unroll
-            for (int u4 = 0; u4 < 8; ++u4)
-              st_shared_v4(box_row + ((static_cast<uint32_t>(u4) ^ static_cast<uint32_t>(row & 7)) << 4),
-                           v[b][4 * u4], v[b][4 * u4 + 1], v[b][4 * u4 + 2], v[b][4 * u4 + 3]);
-          }
+          for (int u4 = 0; u4 < 8; ++u4)
+            st_shared_v4(box_row + ((static_cast<uint32_t>(u4) ^ static_cast<uint32_t>(row & 7)) << 4), v[4 * u4],
+                         v[4 * u4 + 1], v[4 * u4 + 2], v[4 * u4 + 3]);
           fence_proxy_async_smem();
-          bar_sync_n(1, 128);
+          bar_sync_n(1, C::COMPUTE);
           if (threadIdx.x == 0) {
             tma_reduce_add_4d(&tmDQ, sDS, 64 * rnd, i * kB, bh, 0);
             tma_reduce_add_4d(&tmDQ, sDS + C::CHUNK_BYTES, 64 * rnd + 32, i * kB, bh, 0);
@@ -451,7 +465,7 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
       T* dv_row = static_cast<T*>(p.dv) + (head + key) * D;
       T* dk_row = static_cast<T*>(p.dk) + (head + key) * D;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
         uint32_t a[32], b[32];
         tmem_ld32(lane_base + C::TM_DV + 32 * c, a);
         tmem_ld32(lane_base + C::TM_DK + 32 * c, b);
