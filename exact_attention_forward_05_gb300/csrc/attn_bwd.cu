@@ -86,13 +86,16 @@ struct BCfg {
   static constexpr int OFF_D = OFF_LSE + 512;        // 128 floats: D of the query block
   static constexpr int OFF_BAR = OFF_D + 512;
   enum : int { B_KV_FULL = 0, B_KV_EMPTY, B_QD_FULL, B_QD_EMPTY = B_QD_FULL + QD_STAGES,
-               B_SP_FULL = B_QD_EMPTY + QD_STAGES, B_P_READY, B_DQ_FULL, B_DQ_READ, B_EPI_DONE, B_MMA_DONE, NBARS };
+               B_SP_FULL = B_QD_EMPTY + QD_STAGES, B_P_READY, B_DQ_FULL, B_DQ_READ, B_EPI_DONE, B_ACC_FULL,
+               B_MMA_DONE, NBARS };
   static constexpr int USED = OFF_BAR + 8 * NBARS + 16 + 1024;
   // One CTA per SM (TMEM is allocated whole): at least 115 KiB of shared memory.
   static constexpr int SMEM_BYTES = USED > 115 * 1024 ? USED : 115 * 1024;
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-  // TMEM columns: S^T (later P^T in its columns 0-31 and 96-127, then the dQ
-  // partial), dP^T (later dS^T in the same columns of its own), dV, dK.
+  // TMEM columns: S^T (later P^T in its columns 0-31 and 96-127), dP^T (later
+  // dS^T in the same columns of its own), dV, dK.  The dQ partial goes into
+  // the columns the products do not read: d columns 0-63 at S^T + 32, 64-127
+  // at dP^T + 32.
   static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D, TMEM_COLS = 512;
   static_assert(256 + 2 * D <= 512, "S^T, dP^T, dV and dK fit in TMEM");
   // Warps 0-7 compute (warp w: TMEM lanes 32 (w mod 4) .. + 31, column half
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
       constexpr uint32_t fmt = BF16 ? 1u : 0u;
       constexpr uint32_t ID_T = idesc(fmt, kB, kB, 0, 0);   // S^T, dP^T: both operands K-major
       constexpr uint32_t ID_ACC = idesc(fmt, kB, D, 0, 1);  // dV, dK: A from TMEM, B N-major
-      constexpr uint32_t ID_DQ = idesc(fmt, kB, D, 1, 1);   // dQ: A M-major, B N-major
+      constexpr uint32_t ID_DQ = idesc(fmt, kB, 64, 1, 1);  // dQ, 64 columns at a time: A M-major, B N-major
       constexpr uint32_t HI = desc_sw128_hi(1024);
       uint32_t kv_it = 0, qd_it = 0, pr_it = 0, dqr_it = 0, epi_it = 0;
       bool ok = true, first_block = true;
@@ -300,20 +303,27 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
             ++epi_it;
           }
           tc_fence_after();
-          mma_tmem_a(tmem + C::TM_DV, tmem + C::TM_S, sDO(st), i > i0);   // dV += P^T dO
-          mma_tmem_a(tmem + C::TM_DK, tmem + C::TM_DP, sQ(st), i > i0);   // dK += dS^T Q
-          {  // dQ_i = dS K into the S^T columns (after the products above read P^T)
-            const uint32_t a0 = desc_sw128_lo(sDS, C::CHUNK_BYTES), b0 = desc_sw128_lo(sK, C::CHUNK_BYTES);
+          {  // dQ_i = dS K first, into columns no product reads, so the compute
+             // warps read it out while dV and dK are being accumulated
+            const uint32_t a0 = desc_sw128_lo(sDS, C::CHUNK_BYTES);
 #pragma unroll
-            for (int kk = 0; kk < kB / 16; ++kk) {
-              const uint32_t off = (kk * 16 * 128) >> 4;
-              mma_ss_w(tmem + C::TM_S, a0 + off, HI, b0 + off, HI, ID_DQ, kk > 0 ? 1u : 0u, false);
+            for (int hq = 0; hq < D / 64; ++hq) {
+              const uint32_t b0 = desc_sw128_lo(sK + hq * C::CHUNK_BYTES, C::CHUNK_BYTES);
+              const uint32_t dst = tmem + (hq ? C::TM_DP : C::TM_S) + 32;
+#pragma unroll
+              for (int kk = 0; kk < kB / 16; ++kk) {
+                const uint32_t off = (kk * 16 * 128) >> 4;
+                mma_ss_w(dst, a0 + off, HI, b0 + off, HI, ID_DQ, kk > 0 ? 1u : 0u, false);
+              }
             }
           }
-          mma_commit(BAR(C::B_QD_EMPTY + st));
           mma_commit(BAR(C::B_DQ_FULL));
+          mma_tmem_a(tmem + C::TM_DV, tmem + C::TM_S, sDO(st), i > i0);   // dV += P^T dO
+          mma_tmem_a(tmem + C::TM_DK, tmem + C::TM_DP, sQ(st), i > i0);   // dK += dS^T Q
+          mma_commit(BAR(C::B_QD_EMPTY + st));
         }
         if (!ok) break;
+        mma_commit(BAR(C::B_ACC_FULL));  // dV, dK of this unit complete
         mma_commit(BAR(C::B_KV_EMPTY));
         ++units_done;
       }
@@ -327,7 +337,7 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
     const int quad = warp & 3, half = warp >> 2;  // TMEM lane quadrant, column half
     const int row = quad * 32 + lane;  // TMEM lane: key row of S^T, dP^T, dV, dK; query row of dQ
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    uint32_t sp_it = 0, dq_it = 0;
+    uint32_t sp_it = 0, dq_it = 0, acc_it = 0;
     bool ok = true;
     constexpr float kLog2e = 1.4426950408889634f;
     for (int r = 0; ok && r * G < p.num_units; ++r) {
@@ -434,7 +444,7 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
 #pragma unroll 1
         for (int rnd = 0; rnd < D / 64; ++rnd) {
           uint32_t v[32];
-          tmem_ld32(lane_base + C::TM_S + 64 * rnd + 32 * half, v);
+          tmem_ld32(lane_base + (rnd ? C::TM_DP : C::TM_S) + 32 + 32 * half, v);
           tmem_wait_ld(v);
           if (rnd > 0) {
             if (threadIdx.x == 0) bulk_wait_read_all();
@@ -458,8 +468,14 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
         if (lane == 0) mbar_arrive(BAR(C::B_DQ_READ));
       }
       if (!ok) break;
-      // Unit epilogue: dV and scale * dK of this key block (their last
-      // products completed before the last DQ_FULL).
+      // Unit epilogue: dV and scale * dK of this key block, once their last
+      // products have completed.
+      if (bar_red_or(2, C::COMPUTE, !mbar_wait_warp(BAR(C::B_ACC_FULL), acc_it & 1u, wc,
+                                                     attn_internal::kStatusTimeoutSoftmax))) {
+        ok = false;
+        break;
+      }
+      ++acc_it;
       tc_fence_after();
       typedef typename std::conditional<BF16, __nv_bfloat16, __half>::type T;
       T* dv_row = static_cast<T*>(p.dv) + (head + key) * D;
