@@ -324,6 +324,31 @@ def test_prepare_rotation_many_items_per_cta(rope, dtype):
     assert attn.device_status() == attn.ATTN_OK
 
 
+@pytest.mark.parametrize("B, H, N", [(1, 64, 100), (3, 5, 1), (2, 40, 257)])
+@pytest.mark.parametrize("rope", [None, "half"])
+def test_prepare_many_heads_and_short_sequences(B, H, N, rope):
+    """d = 128 streaming pre-pass with the per-unit sign tables: many heads
+    (the table of the next unit's head is filled while the current one is
+    used, wrapping from the last head to the first), sequences shorter than one
+    128-row block, a single row.  Q, K within one E4M3 step of the oracle, V
+    bit-exact."""
+    d = 128
+    q, k, v = synth.outlier_inputs(B, H, N, d, "fp16", seed=16 + H)
+    signs = synth.hadamard_signs(H, d, seed=16 + H)
+    tables = synth.rotary_tables(N, d, offset=1) if rope else None
+    out = attn.fp8_prepare(q.cuda(), k.cuda(), v.cuda(), signs=signs.cuda(),
+                           rope=None if tables is None else tuple(t.cuda() for t in tables))
+    torch.cuda.synchronize()
+    for i, x in enumerate((q, k)):
+        ref = x if tables is None else oracle.rotary(x, *tables, False)
+        codes, scales = oracle.block_quantize(oracle.hadamard_rotate(ref, signs))
+        _assert_codes_within_one_step(_np(out[i]), _np(out[3 + i]), codes, scales)
+    codes, scales = oracle.block_quantize(v)
+    np.testing.assert_array_equal(_np(out[2]), codes)
+    np.testing.assert_array_equal(_np(out[5]), scales)
+    assert attn.device_status() == attn.ATTN_OK
+
+
 def test_prepare_code_buffers_off_32_byte_boundaries():
     """Code buffers that start 16 bytes past a 32-byte boundary take 16-byte
     stores instead of 32-byte ones: the same codes and scales."""
