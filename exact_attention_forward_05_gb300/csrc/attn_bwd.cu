@@ -361,7 +361,10 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
       for (int i = i0; i < p.nkb; ++i) {
         // Stage this block's values for the four warps.  The dS buffer below
         // is also the staging of the last dQ reduce: it must have been read.
-        if (threadIdx.x == 0) bulk_wait_read_all();
+        // Every warp's dQ reduce-adds have read its staging box before dS
+        // overwrites the buffer (the barrier below makes it CTA-wide).
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
         if (bar_red_or(1, C::COMPUTE, !ok)) { ok = false; break; }
         if (half == 0) {  // the first four warps stage the block's lse and D
           lse_s[row] = next_l2;
@@ -437,30 +440,33 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
         if (bar_red_or(2, C::COMPUTE, !got)) { ok = false; break; }
         ++dq_it;
         tc_fence_after();
-        // 64 columns at a time through the dS buffer (free: the dQ product
-        // has read it): each half of the warps stages one 32-float 128-byte
-        // swizzled box, reduce-added into the float32 accumulator (rows past N
-        // are skipped by the copy).
+        // Each warp stages its 32 query rows x 32 columns of a round in its own
+        // 4 KiB box of the dS buffer (free: the dQ product has read it; 128-byte
+        // swizzled rows) and its lane 0 reduce-adds the box into the float32
+        // accumulator (rows past N are skipped by the copy): no barrier across
+        // warps, each warp waits only for its own previous copy.
+        {
+          const uint32_t box = sDS + static_cast<uint32_t>(warp) * 4096u + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll 1
-        for (int rnd = 0; rnd < D / 64; ++rnd) {
-          uint32_t v[32];
-          tmem_ld32(lane_base + (rnd ? C::TM_DP : C::TM_S) + 32 + 32 * half, v);
-          tmem_wait_ld(v);
-          if (rnd > 0) {
-            if (threadIdx.x == 0) bulk_wait_read_all();
-            bar_sync_n(1, C::COMPUTE);
-          }
-          const uint32_t box_row = sDS + static_cast<uint32_t>(half) * C::CHUNK_BYTES + static_cast<uint32_t>(row) * 128u;
+          for (int rnd = 0; rnd < D / 64; ++rnd) {
+            uint32_t v[32];
+            tmem_ld32(lane_base + (rnd ? C::TM_DP : C::TM_S) + 32 + 32 * half, v);
+            tmem_wait_ld(v);
+            if (rnd > 0) {
+              if (lane == 0) bulk_wait_read_all();
+              __syncwarp();
+            }
 #pragma unroll
-          for (int u4 = 0; u4 < 8; ++u4)
-            st_shared_v4(box_row + ((static_cast<uint32_t>(u4) ^ static_cast<uint32_t>(row & 7)) << 4), v[4 * u4],
-                         v[4 * u4 + 1], v[4 * u4 + 2], v[4 * u4 + 3]);
-          fence_proxy_async_smem();
-          bar_sync_n(1, C::COMPUTE);
-          if (threadIdx.x == 0) {
-            tma_reduce_add_4d(&tmDQ, sDS, 64 * rnd, i * kB, bh, 0);
-            tma_reduce_add_4d(&tmDQ, sDS + C::CHUNK_BYTES, 64 * rnd + 32, i * kB, bh, 0);
-            bulk_commit_group();
+            for (int u4 = 0; u4 < 8; ++u4)
+              st_shared_v4(box + ((static_cast<uint32_t>(u4) ^ static_cast<uint32_t>(lane & 7)) << 4), v[4 * u4],
+                           v[4 * u4 + 1], v[4 * u4 + 2], v[4 * u4 + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_4d(&tmDQ, sDS + static_cast<uint32_t>(warp) * 4096u, 64 * rnd + 32 * half,
+                                i * kB + quad * 32, bh, 0);
+              bulk_commit_group();
+            }
           }
         }
         tc_fence_before();
@@ -510,7 +516,7 @@ __global__ void __launch_bounds__(BCfg<D>::THREADS, 1)
   }
 
   // The reduce-adds of dQ must finish before the CTA exits.
-  if (threadIdx.x == 0) bulk_wait_all();
+  if (warp < C::LOAD_WARP && lane == 0) bulk_wait_all();  // each compute warp's own groups
   tc_fence_before();
   __syncthreads();
   if (warp == C::MMA_WARP) {
@@ -581,11 +587,11 @@ attn_status run(const void* q, const void* k, const void* v, const void* o, cons
     return attn_internal::encode_tmap_4d(m, dt, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
   };
   if (!encode(&mq, q) || !encode(&mk, k) || !encode(&mv, v) || !encode(&mdo, dout)) return ATTN_ERR_CUDA;
-  CUtensorMap mdq;  // float32 accumulator [BH, N, d], box 32 floats x 128 rows
+  CUtensorMap mdq;  // float32 accumulator [BH, N, d], box 32 floats x 32 rows (one compute warp's)
   {
     const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(N), static_cast<uint64_t>(BH), 1};
     const uint64_t strides[3] = {D * 4ull, static_cast<uint64_t>(N) * D * 4, static_cast<uint64_t>(BH) * N * D * 4};
-    const uint32_t box[4] = {32, kB, 1, 1};
+    const uint32_t box[4] = {32, 32, 1, 1};
     if (!attn_internal::encode_tmap_4d(&mdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dq_acc, dims, strides, box,
                                        CU_TENSOR_MAP_SWIZZLE_128B))
       return ATTN_ERR_CUDA;
