@@ -299,15 +299,17 @@ __global__ void __launch_bounds__(kPrepThreads, D <= 128 ? 2 : 1) fp8_prepare_ke
 // ---------------------------------------------------------------------------
 // d = 128 with per-block scales: the streaming pre-pass.
 //
-// A persistent grid of two 512-thread CTAs per SM walks the (row block, head)
-// units in contiguous ranges, head fastest, so consecutive units read the same
-// rotary table rows.  A unit is three steps, Q, K and V of its 128 rows, each
-// with its own 32 KiB stage: while a CTA works on one step, each lane already
-// has its row of the next two steps in flight (16-byte asynchronous copies,
-// zero-filled past N, into the lane's own slots of the stage); a step's stage
-// is refilled with the same tensor of the next unit as soon as the step has
-// read it.  The three steps are unrolled, so the code has no branch on the
-// tensor.
+// A persistent grid (two 512-thread CTAs per SM; one when the rotary tables
+// are staged in shared memory) walks the (row block, head) units in
+// contiguous ranges, head fastest, so consecutive units read the same rotary
+// table rows.  A unit is three steps, Q, K and V of its 128 rows, each with its
+// own 32 KiB stage: while a CTA works on one step, each lane already has its
+// row of the next one or two steps in flight (16-byte asynchronous copies,
+// zero-filled past N, into the lane's own slots of the stage); a stage is
+// refilled as soon as its step has read it.  The three steps are unrolled, so
+// the code has no branch on the tensor.  One barrier per Q and K step gathers
+// the block maxima; V has none of its own (its maximum, taken from the 16-bit
+// words in the K step, is published by the K barrier).
 //
 // Row layout over the 4 lanes of its group: lane g holds the four 8-element
 // runs v*32 + g*8 + j (register index e = 8 v + j), so the group's global
@@ -320,10 +322,11 @@ __global__ void __launch_bounds__(kPrepThreads, D <= 128 ? 2 : 1) fp8_prepare_ke
 //
 // With the rotation, 1 / sqrt(d) is folded into the quantisation: the block
 // maximum of the unscaled values times 1 / sqrt(d) (rounding is monotone, so
-// this is the maximum of the scaled values, and s is the same float), then
-// code = RNE_satfinite(x RN(1 / (sqrt(d) s))): one product per value, within a
-// float32 rounding of x / (sqrt(d) s).  Without the rotation the codes keep the
-// FMA-corrected quotient, bit-exact against the float32 division.
+// this is the maximum of the scaled values, and s is the same float), and the
+// codes are RNE_satfinite(x * 448 / amax_unscaled) from the hardware
+// reciprocal, within a few float32 roundings of x / (sqrt(d) s).  Without the
+// rotation the codes keep the FMA-corrected quotient, bit-exact against the
+// float32 division.
 constexpr int kStreamD = 128;
 constexpr int kStreamStageBytes = kQuantRows * kStreamD * 2;  // 32 KiB: one tensor of a unit
 constexpr int kStreamSlotStride = kPrepThreads * 16;          // bytes between a lane's 4 slots
@@ -548,7 +551,7 @@ __global__ void __launch_bounds__(kPrepThreads, ROPE ? 1 : 2) fp8_prepare_stream
       const LaneIds L = lane_ids();
       const int tid = L.tid, warp = L.warp, lane = L.lane, g = L.g, rw = L.rw, rib = L.rib;
       // Refill the stage the previous step read: V of this unit before Q, then
-      // Q and K of the next unit; this step's copies are two groups back.
+      // Q and K of the next unit; this step's copies are two commit groups back.
       if constexpr (T == 0) {
         uint32_t bytes;
         const int r = lane_row(cur, bytes);
