@@ -61,3 +61,12 @@ def test_bwd_ragged_bf16(d, N, causal):
 def test_bwd_b4_h16_n2048_d128(causal):
     """bf16, B=4, H=16, N=2048, d=128: every element of every gradient."""
     _check(4, 16, 2048, 128, "bf16", causal, what=f"B4 H16 N2048 causal={causal}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_fp16_long_ragged(d, causal):
+    """fp16, one head pair with N = 4096 + 37: 33 query blocks per key block (the
+    Q / dO ring and the dQ staging wrap many times within a unit), a ragged
+    last block, every element."""
+    _check(1, 2, 4096 + 37, d, "fp16", causal, seed=40 + d, what=f"fp16 d={d} N=4133 causal={causal}")
