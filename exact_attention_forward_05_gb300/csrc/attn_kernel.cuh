@@ -681,15 +681,27 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         tc_fence_after();
         const uint32_t tm_s = lane_base + (b ? C::TM_S1 : C::TM_S0);
 
+        const bool masked = (p.causal && j >= mask_from) || (j == w.nkb - 1 && (p.Nk % kBN) != 0);
+        // Blocks without masked keys: the loads also give the row's extreme of
+        // each 32-column chunk (maximum, or minimum when the scale is negative).
         uint32_t s[4][32];
+        float ext[4] = {0.f, 0.f, 0.f, 0.f};
+        if (masked) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tm_s + 32 * c, s[c]);
+          for (int c = 0; c < 4; ++c) tmem_ld32(tm_s + 32 * c, s[c]);
+        } else if (cj >= 0.f) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld32_red<false>(tm_s + 32 * c, s[c], ext[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld32_red<true>(tm_s + 32 * c, s[c], ext[c]);
+        }
         tmem_wait_ld(s[0]);
         reg_pin(s[1]);
         reg_pin(s[2]);
         reg_pin(s[3]);
+        reg_pin(ext);
 
-        const bool masked = (p.causal && j >= mask_from) || (j == w.nkb - 1 && (p.Nk % kBN) != 0);
         float mblk;
         if (masked) {
           // Scale first, then mask: t = c*s for visible keys, -inf otherwise.
@@ -706,27 +718,8 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
             }
           mblk = mx;
         } else {
-          float mx;
-          if (cj >= 0.f) {
-            float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-              for (int i = 0; i < 32; i += 8) {
-                m0 = max3(m0, __uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1]));
-                m1 = max3(m1, __uint_as_float(s[c][i + 2]), __uint_as_float(s[c][i + 3]));
-                m2 = max3(m2, __uint_as_float(s[c][i + 4]), __uint_as_float(s[c][i + 5]));
-                m3 = max3(m3, __uint_as_float(s[c][i + 6]), __uint_as_float(s[c][i + 7]));
-              }
-            mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-          } else {
-            mx = INFINITY;
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-              for (int i = 0; i < 32; i += 2)
-                mx = min3(mx, __uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1]));
-          }
+          const float mx = cj >= 0.f ? fmaxf(fmaxf(ext[0], ext[1]), fmaxf(ext[2], ext[3]))
+                                     : fminf(fminf(ext[0], ext[1]), fminf(ext[2], ext[3]));
           mblk = cj * mx;
         }
 

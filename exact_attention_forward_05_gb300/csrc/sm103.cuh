@@ -308,6 +308,32 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 
+// The reducing form of the same load (sm_103a): `ext` receives this thread's
+// maximum (MIN: minimum) of the 32 values it loads.  Like the values, `ext`
+// may be read only after tcgen05.wait::ld (see reg_pin).
+template <bool MIN>
+__device__ __forceinline__ void tmem_ld32_red(uint32_t taddr, uint32_t (&r)[32], float& ext) {
+#define SM103_LD32_RED_OPS                                                                            \
+  "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26," \
+  "%27,%28,%29,%30,%31}, %32, [%33];"
+#define SM103_LD32_RED_OUTS                                                                             \
+  "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),     \
+      "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),        \
+      "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),      \
+      "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),      \
+      "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=f"(ext)
+  if constexpr (MIN)
+    asm volatile("tcgen05.ld.red.sync.aligned.32x32b.x32.min.f32 " SM103_LD32_RED_OPS
+                 : SM103_LD32_RED_OUTS
+                 : "r"(taddr));
+  else
+    asm volatile("tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 " SM103_LD32_RED_OPS
+                 : SM103_LD32_RED_OUTS
+                 : "r"(taddr));
+#undef SM103_LD32_RED_OPS
+#undef SM103_LD32_RED_OUTS
+}
+
 __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;"
                : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
@@ -316,6 +342,12 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
                  "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
                  "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
                  "+r"(r[30]), "+r"(r[31])::"memory");
+}
+
+// Orders later uses of the four reduction results after a preceding
+// tcgen05.wait::ld.
+__device__ __forceinline__ void reg_pin(float (&e)[4]) {
+  asm volatile("" : "+f"(e[0]), "+f"(e[1]), "+f"(e[2]), "+f"(e[3]));
 }
 
 // Orders later uses of `r` after a preceding tcgen05.wait::ld (for fragments
