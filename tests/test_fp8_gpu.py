@@ -156,6 +156,26 @@ def test_fp8_kernel_on_oracle_quantised_operands(N, causal, d):
     assert attn.device_status() == attn.ATTN_OK
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_kernel_negative_scale(causal):
+    """As above with a negative softmax scale: the per-block multiplier of S is
+    negative, so the row extreme taken from S is its minimum."""
+    B, H, N, d = 1, 2, 1100, 128
+    q, k, v = synth.outlier_inputs(B, H, N, d, "bf16", seed=8)
+    (qc, qs), (kc, ks), (vc, vs) = (oracle.block_quantize(t) for t in (q, k, v))
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    scale = -(d ** -0.5)
+    o, lse = attn.attn_fwd_fp8(dev(qc), dev(kc), dev(vc), dev(qs), dev(ks), dev(vs), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.attention(oracle.dequantize(qc, qs), oracle.dequantize(kc, ks),
+                                      oracle.dequantize(vc, vs), causal=causal, scale=scale)
+    diff = o.double().cpu().numpy() - o_ref
+    assert np.isfinite(diff).all()
+    assert np.abs(lse.double().cpu().numpy() - lse_ref).max() <= 1e-3
+    assert np.sqrt(np.mean(diff ** 2)) <= 0.08 * np.sqrt(np.mean(o_ref ** 2))
+    assert attn.device_status() == attn.ATTN_OK
+
+
 @pytest.mark.parametrize("d", PREP_D)
 def test_fp8_weights_layout_through_identity_values(d):
     """V = identity (N = 128 keys, one key block; d = 64 sees the first 64

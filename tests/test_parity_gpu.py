@@ -62,6 +62,16 @@ def test_negative_scale():
         parity.check_case(q, k, v, causal, scale=-0.2, what=f"negative scale causal={causal}")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_negative_scale_many_blocks(dtype):
+    """A negative scale turns the row maximum of scale * S into scale times the
+    row minimum of S: nine key blocks, eight of them without masked keys (the
+    minimum taken by the reducing TMEM load), the last one ragged."""
+    q, k, v = parity.inputs(1, 3, 1100, 128, dtype, seed=15)
+    for causal in (False, True):
+        parity.check_case(q, k, v, causal, scale=-(128 ** -0.5), what=f"negative scale {dtype} causal={causal}")
+
+
 def test_zero_query_gives_mean():
     _, k, v = parity.inputs(1, 2, 200, 64, "bf16", seed=6)
     q = torch.zeros_like(k)
