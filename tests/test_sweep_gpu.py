@@ -8,6 +8,8 @@
   other head.
 * long context: B = 1, H = 16, N = 32768, d = 128, causal, 64 random query
   rows per head plus every row of the last head.
+* longest sequence: B = 1, H = 2, N = 131072, d = 128 (1024 key blocks per
+  row), causal and not, the first and last rows and 62 seeded ones per head.
 Before any slicing, the whole O and lse of the launch are checked to be
 finite, so rows the oracle does not recompute are still covered for NaN or
 infinity.
@@ -78,3 +80,16 @@ def test_long_context_causal():
     rows = synth.sample_rows(N, 64, seed=0, salt=5)
     o, lse = _launch(q, k, v, True, d ** -0.5)
     _check_heads(q, k, v, o, lse, True, d ** -0.5, H - 1, rows, "long context")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_longest_sequence(causal):
+    B, H, N, d = 1, 2, 131072, 128
+    q, k, v = synth.attention_inputs(B, H, N, d, "bf16", seed=3)
+    scale = d ** -0.5
+    rows = np.unique(np.concatenate([[0, N - 1], synth.sample_rows(N, 62, seed=3, salt=11)]))
+    o, lse = _launch(q, k, v, causal, scale)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=causal, scale=scale, rows=rows)
+    idx = torch.as_tensor(rows)
+    parity.assert_close_elementwise(o[:, :, idx], lse[:, :, idx], o_ref, lse_ref, q, k, v, causal, scale,
+                                    rows=rows, what=f"N={N} causal={causal}")
