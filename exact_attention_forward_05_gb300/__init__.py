@@ -22,7 +22,7 @@ import torch
 from . import build as _build
 
 __all__ = ["attn_fwd", "workspace_bytes", "attn_bwd", "bwd_workspace_bytes", "attn_fwd_host", "fp8_prepare", "attn_fwd_fp8", "attn_fwd_fp8_pipeline", "host_workspace_bytes", "device_status",
-           "set_wait_timeout_ns", "set_schedule", "debug_bounded_wait", "debug_fail_host_chunk", "debug_exp2_poly",
+           "set_wait_timeout_ns", "set_schedule", "debug_bounded_wait", "debug_fail_host_chunk", "debug_exp2_poly", "debug_tmem_ld_red",
            "attn_fwd_host_noalloc", "status_string", "library_path",
            "AttnError", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
            "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "exported_symbols",
@@ -109,6 +109,8 @@ def _load():
             lib.attn_debug_bounded_wait.restype = i32
             lib.attn_debug_exp2_poly.argtypes = [vp, vp, vp, i32, vp]
             lib.attn_debug_exp2_poly.restype = i32
+            lib.attn_debug_tmem_ld_red.argtypes = [vp, vp, vp, i32, vp]
+            lib.attn_debug_tmem_ld_red.restype = i32
             lib.attn_debug_fail_host_chunk.argtypes = [i32]
             lib.attn_debug_fail_host_chunk.restype = None
             lib.attn_fwd_host_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp]
@@ -432,6 +434,19 @@ def debug_exp2_poly(x: torch.Tensor):
         _check(_load().attn_debug_exp2_poly(x.data_ptr(), yp.data_ptr(), yr.data_ptr(), x.numel(),
                                             _stream_handle(None, x.device)), "attn_debug_exp2_poly")
     return yp, yr
+
+
+def debug_tmem_ld_red(x: torch.Tensor, use_min: bool = False):
+    """(values, extremes) of a float32 [128, 32] CUDA tensor put into TMEM
+    and read back by the reducing load of the attention softmax: the values
+    unchanged and each row's maximum (minimum with ``use_min``) (a test hook)."""
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous() or tuple(x.shape) != (128, 32):
+        raise ValueError("x must be a contiguous float32 CUDA tensor of shape [128, 32]")
+    vals, ext = torch.empty_like(x), torch.empty(128, dtype=torch.float32, device=x.device)
+    with torch.cuda.device(x.device):
+        _check(_load().attn_debug_tmem_ld_red(x.data_ptr(), vals.data_ptr(), ext.data_ptr(), int(bool(use_min)),
+                                              _stream_handle(None, x.device)), "attn_debug_tmem_ld_red")
+    return vals, ext
 
 
 def debug_fail_host_chunk(chunk: int) -> None:
