@@ -366,8 +366,12 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(dev)
     scale = d ** -0.5
     launches = [0]
+    # With a workspace, full attention takes the stream-K tail (attn_fwd_ws:
+    # the units that do not fill a last round are cut into equal key ranges);
+    # causal launches ignore it.
+    fws = torch.empty(attn.workspace_bytes(d, dev), dtype=torch.uint8, device=dev) if d <= 128 else None
     def step(causal=w["causal"]):
-        attn.attn_fwd(qd, kd, vd, causal=causal, scale=scale, out=o, lse=lse, stream=stream)
+        attn.attn_fwd(qd, kd, vd, causal=causal, scale=scale, out=o, lse=lse, stream=stream, workspace=fws)
         launches[0] += 1
 
     sampler = ClockSampler(local) if rank == 0 else None
@@ -443,8 +447,9 @@ def run_gpu(args):
             "config": {"workload": describe(w), "B": B, "H": H, "N": N, "d": d,
                        "causal": w["causal"], "scale": scale,
                        "flops_per_step_per_gpu": flops(w),
-                       "schedule": "persistent round-robin units" if not w["causal"]
-                                   else "persistent, longest-first causal units",
+                       "schedule": ("persistent round-robin rounds plus a stream-K tail (attn_fwd_ws workspace; "
+                                    "its arrival counters are zeroed by one cudaMemsetAsync before each launch)")
+                                   if not w["causal"] else "persistent, longest-first causal units",
                        "l2": "inputs larger than L2 (Q, K, V, O = 4 x %.0f MiB)" % (B * H * N * d * 2 / 2 ** 20),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": roofline(achieved, traffic=traffic_from_profile(), kernel="attn_fwd_kernel<128, bf16>"),

@@ -1061,13 +1061,10 @@ attn_status launch_fwd(const void* q, const void* k, const void* v, FwdParams pr
   prm.num_units = units;
   prm.stream_k = 0;
   const size_t sk_bytes = stream_k_ws_bytes(D, sms);
-  // Stream-K tail by default only for the FP8 kernel: on the bench shapes it
-  // measured faster there and slower for the 16-bit kernels (whose longer
-  // key-block steps leave the tail less to gain than the parts cost);
-  // ATTN_SCHEDULE_BALANCED takes it for every kind.
+  // Stream-K tail for every kind whenever a workspace is given, except in
+  // the one-tile (no overlap) schedule.
   const int mode = attn_internal::schedule_mode();
-  const bool sk_kind = KIND == KIND_E4M3 || mode == ATTN_SCHEDULE_BALANCED;
-  if (C::NQ == 2 && !prm.causal && ws != nullptr && sk_bytes > 0 && ws_bytes >= sk_bytes && sk_kind &&
+  if (C::NQ == 2 && !prm.causal && ws != nullptr && sk_bytes > 0 && ws_bytes >= sk_bytes &&
       mode != ATTN_SCHEDULE_ONE_TILE && units >= sms && units % sms != 0) {
     // The last `tail` units go to stream-K (at least half a round, so every
     // range holds half a unit's key blocks or more); the rest run in whole

@@ -111,10 +111,10 @@ size_t attn_fwd_workspace_bytes(int d);
  * per CTA (a stream-K tail): a unit cut between CTAs is computed in parts
  * over disjoint key ranges, each writes its unnormalised O and its running
  * maximum and sum to the workspace, and the part that finishes last merges
- * them with the online-softmax rescaling and writes O and lse.  By default
- * only the FP8 kernel takes the tail (see attn_set_schedule); results equal
- * attn_fwd's up to the float32 summation order (FP8: up to the E4M3 rounding
- * of each part's weights).  Causal attention and other shapes run exactly
+ * them with the online-softmax rescaling and writes O and lse.  Every
+ * operand type takes the tail (not under ATTN_SCHEDULE_ONE_TILE); results
+ * equal attn_fwd's up to the float32 summation order (FP8: up to the E4M3
+ * rounding of each part's weights).  Causal attention and other shapes run exactly
  * as attn_fwd.
  *
  *   workspace       : device buffer, 256-byte aligned (else ATTN_ERR_MISALIGNED),
@@ -360,10 +360,9 @@ void attn_set_wait_timeout_ns(uint64_t timeout_ns);
  *   ATTN_SCHEDULE_ONE_TILE: each CTA works on one Q tile at a time (the same
  *       kernel with the second tile idle), so softmax and products of a tile
  *       alternate without overlap.  Same results, bit for bit.
- *   ATTN_SCHEDULE_BALANCED: ping-pong, and calls given a workspace
- *       (attn_fwd_ws, attn_fwd_fp8_ws) take the stream-K tail for every
- *       operand type.  By default only the FP8 kernel takes it: on the
- *       benchmark shapes it measured faster there and slower for fp16/bf16.
+ *   ATTN_SCHEDULE_BALANCED: the same as ATTN_SCHEDULE_PINGPONG (under both,
+ *       calls given a workspace, attn_fwd_ws and attn_fwd_fp8_ws, take the
+ *       stream-K tail for every operand type); kept for callers that set it.
  * Returns ATTN_ERR_INVALID_ARG for any other value (the mode is unchanged).
  */
 #define ATTN_SCHEDULE_PINGPONG 0
