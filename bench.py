@@ -3,7 +3,8 @@
 Default workload: the sequence-length sweep point N = 8192, d = 128 (bf16,
 B = 16384 / N = 2, H = 2048 / d = 16, non-causal; the causal run of the same
 shapes is reported beside it).  A step is one launch of the fused attention
-kernel over that batch.  Metric: attention forward TFLOP/s with
+kernel over that batch, through attn_fwd_ws (its workspace gives full attention
+the stream-K tail; the arrival counters are zeroed by one memset per launch).  Metric: attention forward TFLOP/s with
 FLOPs = 4 B H N^2 d (halved when causal), and its fraction of the measured
 dense BF16 tensor peak.
 
