@@ -302,16 +302,8 @@ STREAM_K_CASES = [(4, 10, 1024, 128, "bf16"), (4, 10, 1000, 64, "fp16"), (2, 20,
                   (1, 33, 2048 + 77, 128, "bf16"), (2, 16, 8192, 128, "bf16")]
 
 
-@pytest.fixture
-def balanced_schedule():
-    """The 16-bit kernels take the stream-K tail only in this mode."""
-    attn.set_schedule(attn.SCHEDULE_BALANCED)
-    yield
-    attn.set_schedule(attn.SCHEDULE_PINGPONG)
-
-
 @pytest.mark.parametrize("case", STREAM_K_CASES)
-def test_stream_k_schedule_matches_oracle(case, balanced_schedule):
+def test_stream_k_schedule_matches_oracle(case):
     B, H, N, d, dt = case
     q, k, v = parity.inputs(B, H, N, d, dt, seed=N + H)
     ws = torch.empty(attn.workspace_bytes(d), dtype=torch.uint8, device="cuda")
@@ -337,7 +329,7 @@ def test_stream_k_schedule_matches_oracle(case, balanced_schedule):
     assert attn.device_status() == attn.ATTN_OK
 
 
-def test_stream_k_repeated_launches_reuse_the_workspace(balanced_schedule):
+def test_stream_k_repeated_launches_reuse_the_workspace():
     """Back-to-back launches on one workspace (the arrival counters are zeroed
     on the stream before each launch): identical results every time."""
     q, k, v = (t.cuda() for t in parity.inputs(4, 10, 1024, 128, "bf16", seed=3))
