@@ -31,8 +31,12 @@ def _check(B, H, N, d, dtype, causal, seed=0, what=""):
     torch.cuda.synchronize()
     assert attn.device_status() == attn.ATTN_OK
     rq, rk, rv = oracle.attention_bwd(q, k, v, g, causal=causal, scale=scale)
+    _assert_grads(((dq, rq), (dk, rk), (dv, rv)), dtype, what)
+
+
+def _assert_grads(pairs, dtype, what):
     u = 2.0 ** -8 if dtype == "bf16" else 2.0 ** -11
-    for name, got, ref in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
+    for name, (got, ref) in zip(("dQ", "dK", "dV"), pairs):
         x = got.double().cpu().numpy()
         assert np.isfinite(x).all(), f"{what} {name}: non-finite"
         e = x - ref
@@ -70,3 +74,23 @@ def test_bwd_fp16_long_ragged(d, causal):
     Q / dO ring and the dQ staging wrap many times within a unit), a ragged
     last block, every element."""
     _check(1, 2, 4096 + 37, d, "fp16", causal, seed=40 + d, what=f"fp16 d={d} N=4133 causal={causal}")
+
+
+def test_bwd_bench_shape_one_head():
+    """bf16, B=2, H=16, N=8192, d=128, non-causal: the backward bench line's
+    launch over the whole problem, and every element of the last head's
+    gradients against the oracle run on that head alone (it sees no other)."""
+    B, H, N, d = 2, 16, 8192, 128
+    q, k, v = parity.inputs(B, H, N, d, "bf16", seed=7)
+    g = synth.attention_inputs(B, H, N, d, "bf16", seed=1007)[0]
+    scale = d ** -0.5
+    qc, kc, vc, gc = q.cuda(), k.cuda(), v.cuda(), g.cuda()
+    o, lse = attn.attn_fwd(qc, kc, vc, scale=scale)
+    dq, dk, dv = attn.attn_bwd(qc, kc, vc, o, gc, lse, scale=scale)
+    torch.cuda.synchronize()
+    assert attn.device_status() == attn.ATTN_OK
+    for t in (dq, dk, dv):
+        assert bool(torch.isfinite(t).all())
+    last = lambda t: t.reshape(1, B * H, N, d)[:, -1:]
+    rq, rk, rv = oracle.attention_bwd(last(q), last(k), last(v), last(g), causal=False, scale=scale)
+    _assert_grads(((last(dq.cpu()), rq), (last(dk.cpu()), rk), (last(dv.cpu()), rv)), "bf16", "bench shape, last head")
