@@ -109,7 +109,7 @@ def _load():
             lib.attn_debug_bounded_wait.restype = i32
             lib.attn_debug_exp2_poly.argtypes = [vp, vp, vp, i32, vp]
             lib.attn_debug_exp2_poly.restype = i32
-            lib.attn_debug_tmem_ld_red.argtypes = [vp, vp, vp, i32, vp]
+            lib.attn_debug_tmem_ld_red.argtypes = [vp, vp, vp, i32, i32, vp]
             lib.attn_debug_tmem_ld_red.restype = i32
             lib.attn_debug_fail_host_chunk.argtypes = [i32]
             lib.attn_debug_fail_host_chunk.restype = None
@@ -437,15 +437,18 @@ def debug_exp2_poly(x: torch.Tensor):
 
 
 def debug_tmem_ld_red(x: torch.Tensor, use_min: bool = False):
-    """(values, extremes) of a float32 [128, 32] CUDA tensor put into TMEM
-    and read back by the reducing load of the attention softmax: the values
-    unchanged and each row's maximum (minimum with ``use_min``) (a test hook)."""
-    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous() or tuple(x.shape) != (128, 32):
-        raise ValueError("x must be a contiguous float32 CUDA tensor of shape [128, 32]")
+    """(values, extremes) of a float32 [128, 32] or [128, 128] CUDA tensor put
+    into TMEM and read back by the reducing load of the attention softmax (its
+    32- or 128-column form): the values unchanged and each row's maximum
+    (minimum with ``use_min``) (a test hook)."""
+    if (x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous() or x.dim() != 2
+            or x.shape[0] != 128 or x.shape[1] not in (32, 128)):
+        raise ValueError("x must be a contiguous float32 CUDA tensor of shape [128, 32] or [128, 128]")
     vals, ext = torch.empty_like(x), torch.empty(128, dtype=torch.float32, device=x.device)
     with torch.cuda.device(x.device):
-        _check(_load().attn_debug_tmem_ld_red(x.data_ptr(), vals.data_ptr(), ext.data_ptr(), int(bool(use_min)),
-                                              _stream_handle(None, x.device)), "attn_debug_tmem_ld_red")
+        _check(_load().attn_debug_tmem_ld_red(x.data_ptr(), vals.data_ptr(), ext.data_ptr(), int(x.shape[1]),
+                                              int(bool(use_min)), _stream_handle(None, x.device)),
+               "attn_debug_tmem_ld_red")
     return vals, ext
 
 

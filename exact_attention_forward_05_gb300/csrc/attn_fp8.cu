@@ -939,16 +939,17 @@ attn_status run_prepare(const PrepParams& prm, int d, int per_tensor, cudaStream
 bool prep_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
 bool fwd_fp8_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
 
-// One CTA of 128 threads: thread r puts row r of x (32 floats) into TMEM lane
-// r and reads it back with the reducing load the attention softmax uses for
-// its row maximum (tmem_ld32_red), then writes the values and the extreme
-// (maximum, or minimum with MIN).
-template <bool MIN>
+// One CTA of 128 threads: thread r puts row r of x (COLS = 32 or 128 floats)
+// into TMEM lane r and reads it back with the reducing load the attention
+// softmax uses for its row maximum (tmem_ld32_red, or tmem_ld128_red for the
+// whole 128-column row), then writes the values and the extreme (maximum, or
+// minimum with MIN).
+template <bool MIN, int COLS>
 __global__ void debug_tmem_red_kernel(const float* x, float* vals, float* ext) {
   __shared__ uint32_t slot;
   const int warp = threadIdx.x >> 5, row = threadIdx.x;
   if (warp == 0) {
-    tmem_alloc(smem_u32(&slot), 32);
+    tmem_alloc(smem_u32(&slot), COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -956,24 +957,34 @@ __global__ void debug_tmem_red_kernel(const float* x, float* vals, float* ext) {
   tc_fence_after();
   const uint32_t tmem = slot;
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-  uint32_t v[32];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(x[row * 32 + i]);
-  tmem_st32(lane_base, v);
+  for (int c = 0; c < COLS / 32; ++c) {
+    uint32_t v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(x[row * COLS + 32 * c + i]);
+    tmem_st32(lane_base + 32 * c, v);
+  }
   tmem_wait_st();
-  uint32_t r[32];
+  uint32_t r[4][32];
   float e[4] = {0.f, 0.f, 0.f, 0.f};
-  tmem_ld32_red<MIN>(lane_base, r, e[0]);
-  tmem_wait_ld(r);
+  if constexpr (COLS == 128)
+    tmem_ld128_red<MIN>(lane_base, r, e[0]);
+  else
+    tmem_ld32_red<MIN>(lane_base, r[0], e[0]);
+  tmem_wait_ld(r[0]);
+#pragma unroll
+  for (int c = 1; c < COLS / 32; ++c) reg_pin(r[c]);
   reg_pin(e);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) vals[row * 32 + i] = __uint_as_float(r[i]);
+  for (int c = 0; c < COLS / 32; ++c)
+#pragma unroll
+    for (int i = 0; i < 32; ++i) vals[row * COLS + 32 * c + i] = __uint_as_float(r[c][i]);
   ext[row] = e[0];
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 32);
+    tmem_dealloc(tmem, COLS);
   }
 }
 
@@ -989,13 +1000,20 @@ namespace attn_internal {
 cudaError_t fp8_status_exchange(unsigned int* out) { return attn_kernel::status_exchange(out); }
 }  // namespace attn_internal
 
-ATTN_EXPORT attn_status attn_debug_tmem_ld_red(const float* x, float* vals, float* ext, int use_min, void* stream) {
-  if (!x || !vals || !ext) return ATTN_ERR_INVALID_ARG;
+ATTN_EXPORT attn_status attn_debug_tmem_ld_red(const float* x, float* vals, float* ext, int cols, int use_min,
+                                              void* stream) {
+  if (!x || !vals || !ext || (cols != 32 && cols != 128)) return ATTN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (use_min)
-    debug_tmem_red_kernel<true><<<1, 128, 0, s>>>(x, vals, ext);
-  else
-    debug_tmem_red_kernel<false><<<1, 128, 0, s>>>(x, vals, ext);
+  if (cols == 128) {
+    if (use_min)
+      debug_tmem_red_kernel<true, 128><<<1, 128, 0, s>>>(x, vals, ext);
+    else
+      debug_tmem_red_kernel<false, 128><<<1, 128, 0, s>>>(x, vals, ext);
+  } else if (use_min) {
+    debug_tmem_red_kernel<true, 32><<<1, 128, 0, s>>>(x, vals, ext);
+  } else {
+    debug_tmem_red_kernel<false, 32><<<1, 128, 0, s>>>(x, vals, ext);
+  }
   return attn_internal::cuda_status(cudaGetLastError());
 }
 

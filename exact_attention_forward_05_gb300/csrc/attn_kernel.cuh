@@ -682,13 +682,24 @@ __global__ void __launch_bounds__(Cfg<D, KIND>::THREADS, 1)
         const uint32_t tm_s = lane_base + (b ? C::TM_S1 : C::TM_S0);
 
         const bool masked = (p.causal && j >= mask_from) || (j == w.nkb - 1 && (p.Nk % kBN) != 0);
-        // Blocks without masked keys: the loads also give the row's extreme of
-        // each 32-column chunk (maximum, or minimum when the scale is negative).
+        // Blocks without masked keys: the loads also give the row's extreme
+        // (maximum, or minimum when the scale is negative): of each 32-column
+        // chunk for the 16-bit kernels, of all 128 columns in one load for E4M3.
         uint32_t s[4][32];
         float ext[4] = {0.f, 0.f, 0.f, 0.f};
         if (masked) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) tmem_ld32(tm_s + 32 * c, s[c]);
+        } else if constexpr (F8) {
+          // One load for the whole row; the other slots hold the identity of
+          // the reduction (ext[0] may be read only after the wait below).
+          if (cj >= 0.f) {
+            tmem_ld128_red<false>(tm_s, s, ext[0]);
+            ext[1] = ext[2] = ext[3] = -INFINITY;
+          } else {
+            tmem_ld128_red<true>(tm_s, s, ext[0]);
+            ext[1] = ext[2] = ext[3] = INFINITY;
+          }
         } else if (cj >= 0.f) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) tmem_ld32_red<false>(tm_s + 32 * c, s[c], ext[c]);

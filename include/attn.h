@@ -405,14 +405,16 @@ attn_status attn_debug_exp2_poly(const float* x, float* y_poly, float* y_ref, in
 /*
  * attn_debug_tmem_ld_red -- test hook for the reducing tensor-memory load
  * (tcgen05.ld.red, sm_103a) from which the attention softmax takes the row
- * maximum of S (the minimum when the scale is negative).  x: 128 x 32 float32
- * (device, row-major); row r goes into TMEM lane r and is read back by that
- * load, which writes the 32 values to vals[r] (device, 128 x 32 floats) and
- * their maximum (use_min = 0) or minimum (use_min != 0) to ext[r] (device, 128
- * floats).  One CTA, 32 TMEM columns; asynchronous on `stream`.
- * ATTN_ERR_INVALID_ARG for a NULL pointer.
+ * maximum of S (the minimum when the scale is negative), in its 32-column
+ * (16-bit kernels) and 128-column (E4M3 kernel) forms.  x: 128 x cols float32
+ * (device, row-major; cols = 32 or 128); row r goes into TMEM lane r and is
+ * read back by that load, which writes the values to vals[r] (device, 128 x
+ * cols floats) and their maximum (use_min = 0) or minimum (use_min != 0) to
+ * ext[r] (device, 128 floats).  One CTA, cols TMEM columns; asynchronous on
+ * `stream`.  ATTN_ERR_INVALID_ARG for a NULL pointer or another cols.
  */
-attn_status attn_debug_tmem_ld_red(const float* x, float* vals, float* ext, int use_min, void* stream);
+attn_status attn_debug_tmem_ld_red(const float* x, float* vals, float* ext, int cols, int use_min,
+                                   void* stream);
 
 /* Last CUDA error code seen by the library (cudaError_t as int; 0 = none). */
 int attn_last_cuda_error(void);
