@@ -258,3 +258,12 @@ def test_bwd_validation_before_launch(lib):
     assert bwd(N=-1) == attn.ATTN_ERR_INVALID_ARG
     assert lib.attn_bwd_workspace_bytes(1, 2, 64, 128) == 1 * 2 * 64 * 128 * 4 + 512
     assert lib.attn_bwd_workspace_bytes(1, 2, 64, 96) == 0
+
+
+def test_debug_tmem_ld_red_validation_before_launch(lib):
+    # Fake, never-dereferenced addresses: a width other than 32 or 128 columns,
+    # or a NULL buffer, is rejected before anything is launched.
+    assert lib.attn_debug_tmem_ld_red(0x1000, 0x2000, 0x3000, 64, 0, None) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_debug_tmem_ld_red(0x1000, 0x2000, 0x3000, 0, 1, None) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_debug_tmem_ld_red(None, 0x2000, 0x3000, 32, 0, None) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_debug_tmem_ld_red(0x1000, 0x2000, None, 128, 0, None) == attn.ATTN_ERR_INVALID_ARG
